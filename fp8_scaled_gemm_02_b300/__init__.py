@@ -1,0 +1,114 @@
+"""B300-native FP8 quantize + scaled-GEMM library (Python binding).
+
+Functions carry the names of the C entry points in include/fp8sgemm.h and
+only marshal torch tensors (device memory, current stream) into them:
+
+  fp8_quantize_per_tensor(x)            -> (q, scale)        one FP32 scale
+  fp8_quantize_token_group(x [M,K])     -> (q, sa [K/128,M]) 1x128 groups
+  fp8_quantize_weight_block(w [N,K])    -> (q, sb [N/128,K/128]) 128x128 blocks
+  fp8_gemm_scaled(qa, sa, qb, sb, ...)  -> C [M,N] FP16/BF16
+
+The path is the FP8 linear layer of "What is FP8 inference on H100
+(Transformer Engine)?" s3 (amax -> scale = amax/448 -> x/scale rounded to
+E4M3 -> FP32-accumulated GEMM -> rescale), with the fine-grained 1x128 /
+128x128 scaling of the transformers "Fine-grained FP8" guide.
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (FP8S_BF16, FP8S_F16, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_TENSOR, Fp8sError, check,
+                   load, status_string)
+
+__all__ = [
+    "fp8_quantize_per_tensor", "fp8_quantize_token_group", "fp8_quantize_weight_block", "fp8_gemm_scaled",
+    "fp8s_device_error", "fp8s_version", "Fp8sError", "status_string", "load", "LIB_PATH",
+    "FP8S_F16", "FP8S_BF16", "FP8S_SCALE_PER_TENSOR", "FP8S_SCALE_BLOCK",
+]
+
+LIB_PATH = _lib.LIB_PATH
+load()  # fail at import time if the CUDA library is missing
+
+_DT = {torch.float16: FP8S_F16, torch.bfloat16: FP8S_BF16}
+_MODE = {"per_tensor": FP8S_SCALE_PER_TENSOR, "block": FP8S_SCALE_BLOCK}
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _in_dtype(t):
+    if t.dtype not in _DT:
+        raise TypeError(f"input must be float16 or bfloat16, got {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def fp8_quantize_per_tensor(x, q=None, scale=None, stream=None):
+    """x (any shape, FP16/BF16) -> (q uint8 same shape, scale float32 [1])."""
+    _need_cuda(x)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if q is None else q
+    scale = torch.empty(4, dtype=torch.float32, device=x.device)[:1] if scale is None else scale
+    st = load().fp8_quantize_per_tensor(_ptr(x), _in_dtype(x), x.numel(), _ptr(q), _ptr(scale), _stream(stream))
+    check(st, "fp8_quantize_per_tensor")
+    return q, scale
+
+
+def fp8_quantize_token_group(x, q=None, sa=None, stream=None):
+    """x [M,K] FP16/BF16 -> (q uint8 [M,K], sa float32 [K/128, M])."""
+    _need_cuda(x)
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+    sa = torch.empty((K // 128, M), dtype=torch.float32, device=x.device) if sa is None else sa
+    st = load().fp8_quantize_token_group(_ptr(x), _in_dtype(x), M, K, _ptr(q), _ptr(sa), _stream(stream))
+    check(st, "fp8_quantize_token_group")
+    return q, sa
+
+
+def fp8_quantize_weight_block(w, q=None, sb=None, stream=None):
+    """w [N,K] FP16/BF16 -> (q uint8 [N,K], sb float32 [ceil(N/128), K/128])."""
+    _need_cuda(w)
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
+    sb = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device) if sb is None else sb
+    st = load().fp8_quantize_weight_block(_ptr(w), _in_dtype(w), N, K, _ptr(q), _ptr(sb), _stream(stream))
+    check(st, "fp8_quantize_weight_block")
+    return q, sb
+
+
+def fp8_gemm_scaled(qa, sa, qb, sb, out_dtype=torch.bfloat16, mode="block", c=None, stream=None):
+    """qa [M,K] uint8, qb [N,K] uint8 -> C [M,N] (FP16/BF16) = rescaled qa.qb^T."""
+    _need_cuda(qa, sa, qb, sb)
+    M, K = qa.shape
+    N = qb.shape[0]
+    if out_dtype not in _DT:
+        raise TypeError("out_dtype must be float16 or bfloat16")
+    c = torch.empty((M, N), dtype=out_dtype, device=qa.device) if c is None else c
+    st = load().fp8_gemm_scaled(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), _ptr(c), _DT[c.dtype], M, N, K,
+                                _MODE[mode], _stream(stream))
+    check(st, "fp8_gemm_scaled")
+    return c
+
+
+def fp8s_device_error(stream=None):
+    """Synchronize and read/clear the device error word (0 = no wait expired)."""
+    where = ctypes.c_int(0)
+    st = load().fp8s_device_error(_stream(stream), ctypes.byref(where))
+    if st not in (0, 6):
+        check(st, "fp8s_device_error")
+    return where.value
+
+
+def fp8s_version():
+    return load().fp8s_version()

@@ -1,0 +1,367 @@
+// fp8sgemm.cu -- the C ABI of libfp8sgemm.so (declared in include/fp8sgemm.h).
+//
+// One translation unit: the kernels (quantize.cuh, gemm.cuh) are included
+// here so the device error word is a single symbol without relocatable
+// device code.  Host code validates arguments, checks the device, encodes
+// (and caches) TMA descriptors, picks a tile configuration and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/fp8sgemm.h"
+#include "gemm.cuh"
+#include "quantize.cuh"
+
+namespace fp8s {
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per mbarrier wait
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(fp8s_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---------------------------------------------------------------- device
+struct DeviceInfo {
+  bool ok = false;
+  bool checked = false;
+  int sms = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+fp8s_status current_device(int* dev_out, DeviceInfo* info_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8S_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return FP8S_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8S_ERR_CUDA;
+    }
+    d.ok = (major == 10 && minor == 3);
+    d.sms = sms;
+    d.checked = true;
+  }
+  if (!d.ok) return FP8S_ERR_UNSUPPORTED_DEVICE;
+  *dev_out = dev;
+  *info_out = d;
+  return FP8S_OK;
+}
+
+fp8s_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8S_OK : FP8S_ERR_CUDA;
+}
+
+// ------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  int64_t rows, cols;
+  int box_rows;
+  int dev;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_rows == o.box_rows && dev == o.dev;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<const void*>()(k.ptr);
+    h ^= std::hash<int64_t>()(k.rows) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    h ^= std::hash<int64_t>()(k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    h ^= std::hash<int>()(k.box_rows * 64 + k.dev) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    return h;
+  }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+std::mutex g_maps_mu;
+
+// Row-major [rows][cols] E4M3 matrix, box of 128 bytes (one K block) x
+// box_rows rows, 128-byte swizzle, out-of-range elements read as zero.
+fp8s_status tensor_map_e4m3(const uint8_t* ptr, int64_t rows, int64_t cols, int box_rows, int dev, CUtensorMap* out) {
+  MapKey key{ptr, rows, cols, box_rows, dev};
+  {
+    std::lock_guard<std::mutex> lk(g_maps_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return FP8S_OK;
+    }
+  }
+  auto fn = encode_fn();
+  if (!fn) return FP8S_ERR_CUDA;
+  CUtensorMap m;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return FP8S_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_maps_mu);
+    if (g_maps.size() > 4096) g_maps.clear();
+    g_maps.emplace(key, m);
+  }
+  *out = m;
+  return FP8S_OK;
+}
+
+// ------------------------------------------------------------ quantizers
+template <int DT>
+fp8s_status launch_token_group(const void* x, int64_t M, int64_t K, uint8_t* q, float* sa, cudaStream_t st,
+                               const DeviceInfo& info) {
+  const int G = static_cast<int>(K / 128);
+  const int64_t row_blocks = (M + 15) / 16;
+  const bool big = row_blocks * G >= 16LL * info.sms * 8;
+  if (big) {
+    dim3 grid(static_cast<unsigned>((row_blocks + 3) / 4), G);
+    quant_token_group_kernel<DT, 4><<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), reinterpret_cast<uint2*>(q),
+                                                          sa, static_cast<int>(M), G);
+  } else {
+    dim3 grid(static_cast<unsigned>(row_blocks), G);
+    quant_token_group_kernel<DT, 1><<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), reinterpret_cast<uint2*>(q),
+                                                          sa, static_cast<int>(M), G);
+  }
+  return launch_status();
+}
+
+template <int DT>
+fp8s_status launch_weight_block(const void* w, int64_t N, int64_t K, uint8_t* q, float* sb, cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>((N + 127) / 128), static_cast<unsigned>(K / 128));
+  quant_weight_block_kernel<DT><<<grid, 256, 0, st>>>(static_cast<const uint4*>(w), reinterpret_cast<uint2*>(q), sb,
+                                                     static_cast<int>(N), static_cast<int>(K / 128));
+  return launch_status();
+}
+
+template <int DT>
+fp8s_status launch_per_tensor(const void* x, int64_t numel, uint8_t* q, float* scale, cudaStream_t st,
+                              const DeviceInfo& info) {
+  const int64_t nvec = numel / 8;
+  const int ntail = static_cast<int>(numel - nvec * 8);
+  const uint16_t* tail = static_cast<const uint16_t*>(x) + nvec * 8;
+  unsigned int* word = reinterpret_cast<unsigned int*>(scale);
+  if (cudaMemsetAsync(word, 0, sizeof(unsigned int), st) != cudaSuccess) return launch_status(), FP8S_ERR_CUDA;
+  int64_t blocks = (nvec + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(info.sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  amax_kernel<DT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint4*>(x), nvec, tail, ntail,
+                                                                  word);
+  cast_per_tensor_kernel<DT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const uint4*>(x), nvec, tail, ntail, reinterpret_cast<uint2*>(q), q + nvec * 8, word);
+  finalize_scale_kernel<<<1, 1, 0, st>>>(word);
+  return launch_status();
+}
+
+// ------------------------------------------------------------------ GEMM
+template <int BN, int MODE, int OUT>
+fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int sms,
+                            cudaStream_t st) {
+  using Cfg = GemmCfg<BN, MODE>;
+  auto kern = fp8_gemm_kernel<BN, MODE, OUT>;
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
+      return launch_status(), FP8S_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
+  return launch_status();
+}
+
+// Tile width: the candidate with the fewest (waves x per-tile cost), where a
+// tile's cost grows with BN plus a fixed part (pipeline fill, epilogue).
+int choose_bn(int64_t M, int64_t N, int mode, int sms) {
+  const int cands_pt[] = {256, 128, 64, 32};
+  const int cands_blk[] = {128, 64, 32};
+  const int* c = mode == FP8S_SCALE_BLOCK ? cands_blk : cands_pt;
+  const int nc = mode == FP8S_SCALE_BLOCK ? 3 : 4;
+  int best = c[0];
+  double best_cost = 1e300;
+  for (int i = 0; i < nc; ++i) {
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + c[i] - 1) / c[i]);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * (c[i] + 32);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c[i];
+    }
+  }
+  return best;
+}
+
+template <int MODE, int OUT>
+fp8s_status dispatch_gemm_bn(int bn, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int sms,
+                             cudaStream_t st) {
+  switch (bn) {
+    case 32: return launch_gemm_cfg<32, MODE, OUT>(ma, mb, p, sms, st);
+    case 64: return launch_gemm_cfg<64, MODE, OUT>(ma, mb, p, sms, st);
+    case 128: return launch_gemm_cfg<128, MODE, OUT>(ma, mb, p, sms, st);
+    case 256:
+      if constexpr (MODE == kModePerTensor) return launch_gemm_cfg<256, MODE, OUT>(ma, mb, p, sms, st);
+      return FP8S_ERR_SHAPE;
+    default: return FP8S_ERR_SHAPE;
+  }
+}
+
+}  // namespace
+}  // namespace fp8s
+
+using namespace fp8s;
+
+extern "C" {
+
+fp8s_status fp8_quantize_per_tensor(const void* x, fp8s_dtype xt, int64_t numel, uint8_t* q, float* scale,
+                                    fp8s_stream_t stream) {
+  if (xt != FP8S_F16 && xt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!x || !q || !scale) return FP8S_ERR_NULL;
+  if (numel < 1) return FP8S_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return xt == FP8S_F16 ? launch_per_tensor<kInF16>(x, numel, q, scale, st, info)
+                        : launch_per_tensor<kInBF16>(x, numel, q, scale, st, info);
+}
+
+fp8s_status fp8_quantize_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K, uint8_t* q, float* sa,
+                                     fp8s_stream_t stream) {
+  if (xt != FP8S_F16 && xt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!x || !q || !sa) return FP8S_ERR_NULL;
+  if (M < 1 || K < 128 || K % 128 != 0 || K / 128 > 65535 || M > (1LL << 31) - 16) return FP8S_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sa)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return xt == FP8S_F16 ? launch_token_group<kInF16>(x, M, K, q, sa, st, info)
+                        : launch_token_group<kInBF16>(x, M, K, q, sa, st, info);
+}
+
+fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int64_t N, int64_t K, uint8_t* q, float* sb,
+                                      fp8s_stream_t stream) {
+  if (wt != FP8S_F16 && wt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!w || !q || !sb) return FP8S_ERR_NULL;
+  if (N < 1 || K < 128 || K % 128 != 0 || K / 128 > 65535 || N > (1LL << 31) - 128) return FP8S_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(sb)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return wt == FP8S_F16 ? launch_weight_block<kInF16>(w, N, K, q, sb, st)
+                        : launch_weight_block<kInBF16>(w, N, K, q, sb, st);
+}
+
+fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, void* c,
+                            fp8s_dtype ct, int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode,
+                            fp8s_stream_t stream) {
+  if (ct != FP8S_F16 && ct != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (mode != FP8S_SCALE_PER_TENSOR && mode != FP8S_SCALE_BLOCK) return FP8S_ERR_DTYPE;
+  if (!qa || !sa || !qb || !sb || !c) return FP8S_ERR_NULL;
+  if (M < 1 || N < 1 || K < 16 || K % 16 != 0) return FP8S_ERR_SHAPE;
+  if (mode == FP8S_SCALE_BLOCK && K % 128 != 0) return FP8S_ERR_SHAPE;
+  if (M > (1LL << 31) - 256 || N > (1LL << 31) - 256 || K > (1LL << 31) - 256 || M * N > (1LL << 40))
+    return FP8S_ERR_SHAPE;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb) || !aligned16(c)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+
+  const int bn = choose_bn(M, N, mode, info.sms);
+  CUtensorMap ma, mb;
+  if (fp8s_status s = tensor_map_e4m3(qa, M, K, kBM, dev, &ma)) return s;
+  if (fp8s_status s = tensor_map_e4m3(qb, N, K, bn, dev, &mb)) return s;
+
+  GemmParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_kb = static_cast<int>((K + kBK - 1) / kBK);
+  p.tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+  p.tiles_n = static_cast<int>((N + bn - 1) / bn);
+  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (tiles > (1LL << 31) - 1) return FP8S_ERR_SHAPE;
+  p.num_tiles = static_cast<int>(tiles);
+  p.group_m = p.tiles_m < 16 ? p.tiles_m : 16;
+  p.sa = sa;
+  p.sb = sb;
+  p.c = c;
+  p.timeout_ns = kWaitTimeoutNs;
+
+  if (mode == FP8S_SCALE_PER_TENSOR)
+    return ct == FP8S_F16 ? dispatch_gemm_bn<kModePerTensor, kOutF16>(bn, ma, mb, p, info.sms, st)
+                          : dispatch_gemm_bn<kModePerTensor, kOutBF16>(bn, ma, mb, p, info.sms, st);
+  return ct == FP8S_F16 ? dispatch_gemm_bn<kModeBlock, kOutF16>(bn, ma, mb, p, info.sms, st)
+                        : dispatch_gemm_bn<kModeBlock, kOutBF16>(bn, ma, mb, p, info.sms, st);
+}
+
+const char* fp8s_status_string(fp8s_status status) {
+  switch (status) {
+    case FP8S_OK: return "ok";
+    case FP8S_ERR_NULL: return "null pointer argument";
+    case FP8S_ERR_SHAPE: return "size out of range or not a required multiple";
+    case FP8S_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP8S_ERR_DTYPE: return "unknown dtype or scale mode";
+    case FP8S_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case FP8S_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
+    case FP8S_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (B300)";
+  }
+  return "unknown status";
+}
+
+fp8s_status fp8s_device_error(fp8s_stream_t stream, int* where) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8S_ERR_CUDA;
+  }
+  unsigned int word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_fp8s_error, sizeof word) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_fp8s_error, &zero, sizeof zero) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8S_ERR_CUDA;
+  }
+  if (where) *where = static_cast<int>(word);
+  return word ? FP8S_ERR_DEVICE_TIMEOUT : FP8S_OK;
+}
+
+int fp8s_version(void) { return kVersion; }
+
+}  // extern "C"

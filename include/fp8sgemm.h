@@ -1,0 +1,143 @@
+/*
+ * fp8sgemm.h -- C ABI of the B300 (sm_103a) FP8 quantize + scaled-GEMM library
+ * (libfp8sgemm.so).
+ *
+ * The path it implements, step by step, is the FP8 linear layer of
+ *   [P2] "What is FP8 inference on H100 (Transformer Engine)?", s3 "How FP8
+ *        inference works" (steps 2-6 and the pseudocode example fp8_gemm):
+ *        amax = max|x|; scale = amax / 448; q = x / scale rounded to E4M3;
+ *        C = (q_A . q_B accumulated in FP32) * scale_A * scale_B -> FP16;
+ *   [P5] "FP8 chi tiet" (transformers fine-grained FP8 guide), opening
+ *        bullets: weights quantized per 128x128 block, activations per token
+ *        per group of 128 input channels.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never frees or keeps them beyond the call (a host-side cache of TMA
+ *    descriptors is keyed by pointer and shape; it holds no device memory).
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and returns once its kernels are enqueued.  Scales are written
+ *    on the device; read them after synchronizing.
+ *  - Arguments are checked on the host before anything is launched; a
+ *    failing check returns its status and has no side effect.  No exception
+ *    crosses the ABI and there is no CPU fallback.
+ *  - The device must be compute capability 10.3 (B300); otherwise
+ *    FP8S_ERR_UNSUPPORTED_DEVICE.  A launch failure gives FP8S_ERR_CUDA.
+ *  - Matrices are row-major with K contiguous: activations A[M][K], weights
+ *    W[N][K] (the nn.Linear layout; C = A * W^T), output C[M][N].
+ *  - E4M3 is the "fn" variant (bias 7, max 448, no infinities); stored
+ *    scales are dequantization factors s = fl32(amax / 448) (s = 1 when
+ *    amax == 0); q = E4M3_rne_satfinite(fl32(x / s)).
+ *  - Every pointer must be 16-byte aligned (FP8S_ERR_ALIGN).
+ */
+#ifndef FP8SGEMM_H
+#define FP8SGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8S_API __attribute__((visibility("default")))
+#else
+#define FP8S_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* fp8s_stream_t;
+
+typedef enum {
+  FP8S_OK = 0,
+  FP8S_ERR_NULL = 1,               /* a required pointer is NULL */
+  FP8S_ERR_SHAPE = 2,              /* a size is out of range or breaks a multiple-of rule */
+  FP8S_ERR_ALIGN = 3,              /* a pointer is not 16-byte aligned */
+  FP8S_ERR_DTYPE = 4,              /* unknown dtype or scale-mode value */
+  FP8S_ERR_CUDA = 5,               /* a CUDA runtime/driver call or launch failed */
+  FP8S_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait gave up (see fp8s_device_error) */
+  FP8S_ERR_UNSUPPORTED_DEVICE = 7  /* current device is not compute capability 10.3 */
+} fp8s_status;
+
+typedef enum { FP8S_F16 = 0, FP8S_BF16 = 1 } fp8s_dtype;
+
+typedef enum {
+  FP8S_SCALE_PER_TENSOR = 0, /* sa, sb each point to one float */
+  FP8S_SCALE_BLOCK = 1       /* sa: [K/128][M] token-group scales, sb: [ceil(N/128)][K/128] block scales */
+} fp8s_scale_mode;
+
+/*
+ * fp8_quantize_per_tensor -- [P2] s3 steps 2-4 with one scale per tensor.
+ *   x      [numel] FP16/BF16 (xt), device.            numel >= 1.
+ *   q      [numel] E4M3 bytes, device (output).
+ *   scale  one float, device (output): s = fl32(max|x| / 448), 1 if all zero.
+ * Two passes over x (an amax reduction, then the cast).  `scale` is used as
+ * the reduction's accumulator while the call runs; its final value is s.
+ */
+FP8S_API fp8s_status fp8_quantize_per_tensor(const void* x, fp8s_dtype xt, int64_t numel,
+                                    uint8_t* q, float* scale, fp8s_stream_t stream);
+
+/*
+ * fp8_quantize_token_group -- [P5] per-token 1x128 activation groups, each
+ * group quantized as in [P2] s3 steps 2-4.  One read of x.
+ *   x   [M][K] FP16/BF16 (xt), device.   M >= 1, K >= 128, K % 128 == 0.
+ *   q   [M][K] E4M3 bytes, device (output).
+ *   sa  [K/128][M] floats, device (output): sa[g*M + m] is the scale of
+ *       x[m][128g .. 128g+127].  (Group-major so the GEMM reads 128
+ *       consecutive token scales per K block.)
+ */
+FP8S_API fp8s_status fp8_quantize_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K,
+                                     uint8_t* q, float* sa, fp8s_stream_t stream);
+
+/*
+ * fp8_quantize_weight_block -- [P5] 128x128 weight blocks (weight_block_size
+ * = (128, 128)), each quantized as in [P2] s3 steps 2-4.  One read of w.
+ *   w   [N][K] FP16/BF16 (wt), device.   N >= 1, K >= 128, K % 128 == 0.
+ *   q   [N][K] E4M3 bytes, device (output).
+ *   sb  [ceil(N/128)][K/128] floats, device (output): sb[i*(K/128) + j] is the
+ *       scale of rows 128i.. (the valid ones only, for a ragged last block)
+ *       and columns 128j..128j+127.
+ */
+FP8S_API fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int64_t N, int64_t K,
+                                      uint8_t* q, float* sb, fp8s_stream_t stream);
+
+/*
+ * fp8_gemm_scaled -- [P2] s3 steps 5-6: C = (qa . qb^T, FP32 accumulation on
+ * the tensor cores) rescaled by the operand scales, rounded to nearest-even
+ * into FP16/BF16 (ct).
+ *   qa  [M][K] E4M3, device.   qb [N][K] E4M3, device.   c [M][N] output, device.
+ *   mode FP8S_SCALE_PER_TENSOR: sa, sb -> one float each;
+ *        C[m][n] = RN(acc[m][n] * sa * sb).          K % 16 == 0.
+ *   mode FP8S_SCALE_BLOCK ([P5] block geometry): sa [K/128][M], sb
+ *        [ceil(N/128)][K/128]; each 128-wide K block's FP32 partial sum is
+ *        multiplied by sa[kb][m] * sb[n/128][kb] and added into an FP32
+ *        accumulator;  C[m][n] = RN(acc).             K % 128 == 0.
+ *   M, N >= 1, K >= 16.  N need not be a multiple of anything.
+ */
+FP8S_API fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                            void* c, fp8s_dtype ct, int64_t M, int64_t N, int64_t K,
+                            fp8s_scale_mode mode, fp8s_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+FP8S_API const char* fp8s_status_string(fp8s_status status);
+
+/*
+ * fp8s_device_error -- synchronizes `stream`, then reads and clears the
+ * current device's error word, which a kernel sets when one of its bounded
+ * waits gives up (the kernel then exits without finishing its output).
+ * *where (if not NULL) receives the word: 0 if no wait gave up, else
+ * 1 = TMA producer, 2 = MMA issuer, 3 = epilogue.  Returns FP8S_OK,
+ * FP8S_ERR_DEVICE_TIMEOUT or FP8S_ERR_CUDA.
+ */
+FP8S_API fp8s_status fp8s_device_error(fp8s_stream_t stream, int* where);
+
+/* Library version, major*10000 + minor*100 + patch. */
+FP8S_API int fp8s_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8SGEMM_H */

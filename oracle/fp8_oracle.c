@@ -265,6 +265,11 @@ void oracle_quantize_weight_block(const uint16_t* w, int dtype, int64_t N, int64
 
 static int64_t row_of(const int64_t* rows, int64_t i) { return rows ? rows[i] : i; }
 
+/* dec[b] = oracle_e4m3_decode(b) for all 256 codes (a lookup of O1). */
+static void decode_table(double* dec) {
+  for (int b = 0; b < 256; ++b) dec[b] = oracle_e4m3_decode((uint8_t)b);
+}
+
 /* Per-tensor scaled GEMM [P2 s3 steps 5-6 and pseudocode, R6]:
  *   R[i][n] = (sum_k dec(qa[m][k]) * dec(qb[n][k])) * sa * sb,  m = rows[i].
  * qa: [M][K], qb: [N][K] (weight layout, so C = A * W^T).  R: [nrows][N].
@@ -273,13 +278,15 @@ static int64_t row_of(const int64_t* rows, int64_t i) { return rows ? rows[i] : 
 void oracle_gemm_per_tensor(const uint8_t* qa, float sa, const uint8_t* qb, float sb,
                             int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
                             double* R) {
+  double dec[256];
+  decode_table(dec);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < nrows; ++i) {
     int64_t m = row_of(rows, i);
     for (int64_t n = 0; n < N; ++n) {
       double acc = 0.0;
       for (int64_t k = 0; k < K; ++k)
-        acc += oracle_e4m3_decode(qa[m * K + k]) * oracle_e4m3_decode(qb[n * K + k]);
+        acc += dec[qa[m * K + k]] * dec[qb[n * K + k]];
       R[i * N + n] = acc * (double)sa * (double)sb;
     }
   }
@@ -292,6 +299,8 @@ void oracle_gemm_block(const uint8_t* qa, const float* sa, int64_t M_total,
                        const uint8_t* qb, const float* sb, int64_t N, int64_t K,
                        const int64_t* rows, int64_t nrows, double* R) {
   int64_t KB = K / 128;
+  double dec[256];
+  decode_table(dec);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < nrows; ++i) {
     int64_t m = row_of(rows, i);
@@ -300,7 +309,7 @@ void oracle_gemm_block(const uint8_t* qa, const float* sa, int64_t M_total,
       for (int64_t kb = 0; kb < KB; ++kb) {
         double part = 0.0;
         for (int64_t k = kb * 128; k < kb * 128 + 128; ++k)
-          part += oracle_e4m3_decode(qa[m * K + k]) * oracle_e4m3_decode(qb[n * K + k]);
+          part += dec[qa[m * K + k]] * dec[qb[n * K + k]];
         acc += part * (double)sa[kb * M_total + m] * (double)sb[(n / 128) * KB + kb];
       }
       R[i * N + n] = acc;

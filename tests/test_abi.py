@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every entry point its header declares,
+and rejects bad arguments on the host before touching the GPU (these calls
+return before any CUDA call, so they run on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_scaled_gemm_02_b300 import build
+    build.build()
+    from fp8_scaled_gemm_02_b300 import _lib
+    return _lib.load()
+
+
+def declared_symbols():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            names += re.findall(r"FP8S_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_the_four_calls():
+    names = declared_symbols()
+    for n in ("fp8_quantize_per_tensor", "fp8_quantize_token_group", "fp8_quantize_weight_block",
+              "fp8_gemm_scaled"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_binding_covers_header(lib):
+    from fp8_scaled_gemm_02_b300 import _lib
+    assert set(declared_symbols()) == set(_lib.SIGNATURES)
+
+
+def test_status_strings_and_version(lib):
+    from fp8_scaled_gemm_02_b300 import _lib
+    for code in range(8):
+        s = _lib.status_string(code)
+        assert s and s != "unknown status"
+    assert _lib.status_string(99) == "unknown status"
+    assert lib.fp8s_version() >= 100
+
+
+P = ctypes.c_void_p
+GOOD = P(1 << 20)      # a 16-byte aligned non-null address; never dereferenced
+BAD_ALIGN = P((1 << 20) + 8)
+
+
+def test_quantize_argument_checks(lib):
+    # dtype is checked first, then pointers, then sizes, then alignment
+    assert lib.fp8_quantize_token_group(GOOD, 7, 128, 128, GOOD, GOOD, None) == 4
+    assert lib.fp8_quantize_token_group(None, 0, 128, 128, GOOD, GOOD, None) == 1
+    assert lib.fp8_quantize_token_group(GOOD, 0, 128, 100, GOOD, GOOD, None) == 2
+    assert lib.fp8_quantize_token_group(GOOD, 0, 0, 128, GOOD, GOOD, None) == 2
+    assert lib.fp8_quantize_token_group(GOOD, 0, 128, 128, BAD_ALIGN, GOOD, None) == 3
+    assert lib.fp8_quantize_weight_block(GOOD, 1, 0, 128, GOOD, GOOD, None) == 2
+    assert lib.fp8_quantize_weight_block(GOOD, 1, 5, 129, GOOD, GOOD, None) == 2
+    assert lib.fp8_quantize_weight_block(GOOD, 1, 5, 128, GOOD, None, None) == 1
+    assert lib.fp8_quantize_weight_block(BAD_ALIGN, 1, 5, 128, GOOD, GOOD, None) == 3
+    assert lib.fp8_quantize_per_tensor(GOOD, 0, 0, GOOD, GOOD, None) == 2
+    assert lib.fp8_quantize_per_tensor(GOOD, 2, 10, GOOD, GOOD, None) == 4
+    assert lib.fp8_quantize_per_tensor(GOOD, 0, 10, GOOD, BAD_ALIGN, None) == 3
+
+
+def test_gemm_argument_checks(lib):
+    g = lib.fp8_gemm_scaled
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 3, 1, 1, 16, 0, None) == 4          # out dtype
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 1, 1, 16, 5, None) == 4          # scale mode
+    assert g(GOOD, None, GOOD, GOOD, GOOD, 0, 1, 1, 16, 0, None) == 1
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 0, 1, 16, 0, None) == 2          # M < 1
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 1, 1, 24, 0, None) == 2          # K % 16
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 1, 1, 144, 1, None) == 2         # block: K % 128
+    assert g(GOOD, GOOD, GOOD, GOOD, BAD_ALIGN, 0, 1, 1, 16, 0, None) == 3
+
+
+def test_oracle_is_not_linked_into_the_library(lib):
+    """The product library neither exports nor imports any oracle symbol."""
+    import subprocess
+    from fp8_scaled_gemm_02_b300 import _lib
+    out = subprocess.run(["nm", "-D", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    assert "oracle_" not in out
+    src = open(os.path.join(ROOT, "fp8_scaled_gemm_02_b300", "__init__.py")).read()
+    assert "oracle" not in src.replace("no fallback", "")
