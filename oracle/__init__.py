@@ -232,13 +232,24 @@ def dot_units(qa, qb, k0=0, k1=None) -> np.ndarray:
 
 
 def within_tolerance(C, R, out_dtype):
-    """The parity bar for GEMM outputs: |C - R| <= t*|R| + t*rms(R), t = 1e-3
-    for FP16 output and 2e-3 for BF16.  Returns (ok, worst ratio)."""
-    t = 2e-3 if _dt(out_dtype) == BF16 else 1e-3
+    """The parity bar for GEMM outputs, against the unrounded FP64 result R:
+        FP16 output:  |C - R| <= 1e-3*|R| + 1e-3*rms(R)
+        BF16 output:  |C - R| <= 2e-3*|R| + 2e-3*rms(R) + ulp_bf16(R)/2
+    The BF16 half-ulp term is the error of rounding R itself to BF16 to
+    nearest (up to 2^-8*|R|, more than 2e-3*|R|), which no implementation can
+    avoid; FP16's half-ulp (<= 2^-11*|R|) already fits inside its bound.
+    Returns (ok, worst error / bound)."""
+    bf16 = _dt(out_dtype) == BF16
+    t = 2e-3 if bf16 else 1e-3
     C = np.asarray(C, np.float64)
     R = np.asarray(R, np.float64)
-    rms = float(np.sqrt(np.mean(R * R))) if R.size else 0.0
+    if R.size == 0:
+        return True, 0.0
+    rms = float(np.sqrt(np.mean(R * R)))
     bound = t * np.abs(R) + t * rms
+    if bf16:
+        _, e = np.frexp(R)                       # |R| = f * 2^e, f in [0.5, 1)
+        bound = bound + np.ldexp(1.0, np.maximum(e, -125) - 9)   # half of 2^(e-1-7)
     err = np.abs(C - R)
-    ratio = float(np.max(err / np.maximum(bound, 1e-300))) if R.size else 0.0
+    ratio = float(np.max(err / np.maximum(bound, 1e-300)))
     return bool(np.all(err <= bound)), ratio

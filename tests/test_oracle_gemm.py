@@ -123,3 +123,17 @@ def test_tolerance_helper():
     assert not ok
     ok, _ = o.within_tolerance(R * (1 + 1.9e-3), R, "bf16")
     assert ok
+    # BF16: rounding the exact result itself to BF16 must always pass
+    rng = np.random.default_rng(0)
+    R = rng.standard_normal(100000) * 3.0
+    R[:10] = 1.0 + 2.0 ** -8 * 0.999        # just below a rounding midpoint above 1
+    Cb = torch.from_numpy(R).to(torch.bfloat16).double().numpy()
+    ok, ratio = o.within_tolerance(Cb, R, "bf16")
+    assert ok, ratio
+    Ch = R.astype(np.float16).astype(np.float64)
+    assert o.within_tolerance(Ch, R, "f16")[0]
+    # ... but being two BF16 ulps off at a large value does not
+    Cbad = Cb.copy()
+    k = int(np.argmax(np.abs(R)))
+    Cbad[k] = Cb[k] + np.sign(R[k]) * 2.0 * 2.0 ** (np.frexp(R[k])[1] - 8)
+    assert not o.within_tolerance(Cbad, R, "bf16")[0]
