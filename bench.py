@@ -11,10 +11,12 @@ inputs that consecutive uses of one copy are more than 2x the L2 size apart.
 
 Timed regions (CUDA events on the launching stream, synchronize + barrier on
 both sides, max over ranks):
-  step region:   K steps, each one CUDA-graph launch of the step's kernels.
-  kernel region: the same K steps launched kernel by kernel (one graph per
-                 kernel), with an event after every kernel; per-kernel average
-                 durations feed the `roofline` object and `kernels`.
+  step region:   exactly K steps, replayed as CUDA graphs of many steps so
+                 host launch cost never paces the GPU.
+  kernel region: every kernel of the step alone, min(K, 2048) back-to-back
+                 launches (rotating input sets) in one CUDA graph between two
+                 events; these per-launch durations feed `roofline` and
+                 `kernels`.
   e2e region:    K steps through the public API with host buffers: H2D of A
                  and W from pinned memory, the path, D2H of C.
 
@@ -53,6 +55,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped to ~2 s")
+    p.add_argument("--modes", default="", help="override the workload's scaling modes, e.g. per_tensor,block")
+    p.add_argument("--profile", type=int, default=0,
+                   help="run N eager steps on one input set and exit (a small command for ncu captures)")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -235,6 +240,9 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
 
     wl = synth.WORKLOADS[args.workload]
+    if args.modes:
+        import dataclasses
+        wl = dataclasses.replace(wl, modes=tuple(args.modes.split(",")))
     plan = kernel_plan(wl)
     td = {"f16": torch.float16, "bf16": torch.bfloat16}
     in_t, out_t = td[wl.in_dtype], td[wl.out_dtype]
@@ -260,6 +268,8 @@ def run_ours(args):
         pass
     R = max(2, math.ceil(2 * l2 / set_bytes) + 1)
     R = min(R, max(2, int(40e9 // set_bytes)))
+    if args.profile:
+        R = 1
 
     sets = []
     for r in range(R):
@@ -308,23 +318,45 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert F.fp8s_device_error() == 0
 
-    # CUDA graphs: one per (set, kernel) and one per set for the whole step
+    if args.profile:
+        for _ in range(args.profile - 1):
+            for c in kernel_calls(0):
+                c()
+        torch.cuda.synchronize()
+        assert F.fp8s_device_error() == 0
+        if rank == 0:
+            print(json.dumps({"profile_steps": args.profile, "workload": args.workload, "modes": list(wl.modes),
+                              "kernels_per_step": len(kinfo)}))
+        return
+
+    # CUDA graphs.  Host launch cost must never pace the GPU, so each timed
+    # region is one or a few graph launches:
+    #   step region:   a graph of C consecutive steps (C a multiple of R),
+    #                  replayed K // C times, plus a graph of the K % C rest;
+    #   kernel region: per kernel of the step, one graph of Kk = min(K, 2048)
+    #                  back-to-back launches of that kernel alone.
     stream = torch.cuda.Stream(device=dev)
-    kgraphs, sgraphs = [], []
+    nk = len(kinfo)
+
+    def capture(steps, only=None):
+        """Graph of `steps` consecutive steps (rotating input sets); with
+        `only` = j, just kernel j of each step."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                for j, c in enumerate(kernel_calls(i % R)):
+                    if only is None or only == j:
+                        c()
+        return g
+
+    K, W = args.steps, args.warmup
+    C = min(K, max(R, (256 // R) * R))
+    Kk = min(K, 2048)
     with torch.cuda.stream(stream):
-        for r in range(R):
-            row = []
-            for c in kernel_calls(r):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    c()
-                row.append(g)
-            kgraphs.append(row)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for c in kernel_calls(r):
-                    c()
-            sgraphs.append(g)
+        g_one = capture(1)
+        g_chunk = capture(C)
+        g_rest = capture(K % C) if K % C else None
+        g_kern = [capture(Kk, only=j) for j in range(nk)]
     torch.cuda.synchronize()
 
     def barrier():
@@ -342,52 +374,41 @@ def run_ours(args):
     sampler = ClockSampler(local)
     if sampler.ok:
         sampler.start()
-    K, W = args.steps, args.warmup
     t_wide0 = time.perf_counter()
     with torch.cuda.stream(stream):
         # spin-up: ~0.3 s of steps so clocks settle and the sampler sees load
         t_end = time.perf_counter() + 0.3
-        i = 0
         while time.perf_counter() < t_end:
-            sgraphs[i % R].replay()
-            i += 1
-            if i % 64 == 0:
-                stream.synchronize()
+            g_chunk.replay()
+            stream.synchronize()
         for i in range(W):
-            sgraphs[i % R].replay()
+            g_one.replay()
         barrier()
 
-        # ---- step region
+        # ---- step region: exactly K steps
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         ev0.record(stream)
-        for i in range(K):
-            sgraphs[i % R].replay()
+        for _ in range(K // C):
+            g_chunk.replay()
+        if g_rest is not None:
+            g_rest.replay()
         ev1.record(stream)
         barrier()
         t1 = time.perf_counter()
         step_ms = max_over_ranks(ev0.elapsed_time(ev1)) / K
 
-        # ---- kernel region
-        nk = len(kinfo)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
-        for i in range(W):
-            for g in kgraphs[i % R]:
-                g.replay()
-        barrier()
-        for i in range(K):
-            row = kgraphs[i % R]
-            e = evs[i]
-            e[0].record(stream)
-            for j in range(nk):
-                row[j].replay()
-                e[j + 1].record(stream)
-        barrier()
-        kern_ms = [0.0] * nk
-        for i in range(K):
-            for j in range(nk):
-                kern_ms[j] += evs[i][j].elapsed_time(evs[i][j + 1])
-        kern_ms = [max_over_ranks(x / K) for x in kern_ms]
+        # ---- kernel region: each kernel alone, Kk back-to-back launches
+        kern_ms = []
+        for j in range(nk):
+            g_kern[j].replay()   # untimed pass
+            barrier()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            g_kern[j].replay()
+            eb.record(stream)
+            barrier()
+            kern_ms.append(max_over_ranks(ea.elapsed_time(eb)) / Kk)
         kregion_step_ms = sum(kern_ms)
     sampler.stop_flag.set()
     assert F.fp8s_device_error() == 0, "a kernel's bounded wait expired during the benchmark"
@@ -488,7 +509,9 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "kernels": kernels,
-        "kernel_region_ms_per_step": round(kregion_step_ms, 6),
+        "kernel_region": {"steps": Kk, "ms_per_step": round(kregion_step_ms, 6),
+                          "timing": "each kernel alone: one CUDA graph of back-to-back launches over the "
+                                    "rotating input sets, CUDA events around it"},
         "gpu_launches": K * sum(launches_per_kernel),
         "e2e": e2e,
         "clocks": sampler.summary(t0, t1, t_wide0),

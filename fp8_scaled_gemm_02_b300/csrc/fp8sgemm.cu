@@ -89,28 +89,32 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapKey {
   const void* ptr;
   int64_t rows, cols;
-  int box_rows;
+  int box_rows, box_cols, elem_bytes, swizzle;
   int dev;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_rows == o.box_rows && dev == o.dev;
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_rows == o.box_rows && box_cols == o.box_cols &&
+           elem_bytes == o.elem_bytes && swizzle == o.swizzle && dev == o.dev;
   }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     size_t h = std::hash<const void*>()(k.ptr);
-    h ^= std::hash<int64_t>()(k.rows) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
-    h ^= std::hash<int64_t>()(k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
-    h ^= std::hash<int>()(k.box_rows * 64 + k.dev) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    auto mix = [&h](size_t v) { h ^= v + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2); };
+    mix(std::hash<int64_t>()(k.rows));
+    mix(std::hash<int64_t>()(k.cols));
+    mix(static_cast<size_t>(k.box_rows) * 1000003u + static_cast<size_t>(k.box_cols) * 131u +
+        static_cast<size_t>(k.elem_bytes) * 7u + static_cast<size_t>(k.swizzle) + static_cast<size_t>(k.dev) * 65537u);
     return h;
   }
 };
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 std::mutex g_maps_mu;
 
-// Row-major [rows][cols] E4M3 matrix, box of 128 bytes (one K block) x
-// box_rows rows, 128-byte swizzle, out-of-range elements read as zero.
-fp8s_status tensor_map_e4m3(const uint8_t* ptr, int64_t rows, int64_t cols, int box_rows, int dev, CUtensorMap* out) {
-  MapKey key{ptr, rows, cols, box_rows, dev};
+// Row-major [rows][cols] matrix of 1- or 2-byte elements; box of
+// box_cols x box_rows elements; out-of-range elements read as zero.
+fp8s_status tensor_map_2d(const void* ptr, int64_t rows, int64_t cols, int elem_bytes, int box_rows, int box_cols,
+                          bool swizzle128, int dev, CUtensorMap* out) {
+  MapKey key{ptr, rows, cols, box_rows, box_cols, elem_bytes, swizzle128 ? 1 : 0, dev};
   {
     std::lock_guard<std::mutex> lk(g_maps_mu);
     auto it = g_maps.find(key);
@@ -123,12 +127,13 @@ fp8s_status tensor_map_e4m3(const uint8_t* ptr, int64_t rows, int64_t cols, int 
   if (!fn) return FP8S_ERR_CUDA;
   CUtensorMap m;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * elem_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return FP8S_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lk(g_maps_mu);
@@ -136,6 +141,24 @@ fp8s_status tensor_map_e4m3(const uint8_t* ptr, int64_t rows, int64_t cols, int 
     g_maps.emplace(key, m);
   }
   *out = m;
+  return FP8S_OK;
+}
+
+// E4M3 operand of the GEMM: boxes of one 128-byte K block x box_rows rows,
+// 128-byte swizzle (the layout the MMA's shared-memory descriptors expect).
+fp8s_status tensor_map_e4m3(const uint8_t* ptr, int64_t rows, int64_t cols, int box_rows, int dev, CUtensorMap* out) {
+  return tensor_map_2d(ptr, rows, cols, 1, box_rows, kBK, true, dev, out);
+}
+
+template <typename KernelT>
+fp8s_status ensure_smem_attr(KernelT kern, int bytes, bool* done_per_device) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return launch_status(), FP8S_ERR_CUDA;
+  if (!done_per_device[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return launch_status(), FP8S_ERR_CUDA;
+    done_per_device[dev] = true;
+  }
   return FP8S_OK;
 }
 
@@ -159,10 +182,18 @@ fp8s_status launch_token_group(const void* x, int64_t M, int64_t K, uint8_t* q, 
 }
 
 template <int DT>
-fp8s_status launch_weight_block(const void* w, int64_t N, int64_t K, uint8_t* q, float* sb, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>((N + 127) / 128), static_cast<unsigned>(K / 128));
-  quant_weight_block_kernel<DT><<<grid, 256, 0, st>>>(static_cast<const uint4*>(w), reinterpret_cast<uint2*>(q), sb,
-                                                     static_cast<int>(N), static_cast<int>(K / 128));
+fp8s_status launch_weight_block(const void* w, int64_t N, int64_t K, uint8_t* q, float* sb, cudaStream_t st,
+                                const DeviceInfo& info, int dev) {
+  CUtensorMap mw;
+  if (fp8s_status s = tensor_map_2d(w, N, K, 2, 128, 128, false, dev, &mw)) return s;
+  static bool attr_done[kMaxDevices] = {};
+  auto kern = quant_weight_block_tma_kernel<DT>;
+  if (fp8s_status s = ensure_smem_attr(kern, kWbSmemBytes, attr_done)) return s;
+  const int64_t nblocks = ((N + 127) / 128) * (K / 128);
+  const int64_t cap = 2LL * info.sms;
+  const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
+  kern<<<grid, 288, kWbSmemBytes, st>>>(mw, reinterpret_cast<uint2*>(q), sb, static_cast<int>(N),
+                                         static_cast<int>(K / 128), static_cast<int>(nblocks), kWaitTimeoutNs);
   return launch_status();
 }
 
@@ -193,31 +224,28 @@ fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const 
   using Cfg = GemmCfg<BN, MODE>;
   auto kern = fp8_gemm_kernel<BN, MODE, OUT>;
   static bool attr_set[kMaxDevices] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
-      return launch_status(), FP8S_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  if (fp8s_status s = ensure_smem_attr(kern, Cfg::kSmemBytes, attr_set)) return s;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
   return launch_status();
 }
 
-// Tile width: the candidate with the fewest (waves x per-tile cost), where a
-// tile's cost grows with BN plus a fixed part (pipeline fill, epilogue).
+// Tile width: the candidate with the fewest (waves x per-tile cost).  A
+// tile's cost is its width divided by the tensor-pipe efficiency measured for
+// that width on the B300 (narrow tiles are bound by shared-memory operand
+// traffic, not by the MMA), plus a fixed part (pipeline fill, epilogue).
 int choose_bn(int64_t M, int64_t N, int mode, int sms) {
   const int cands_pt[] = {256, 128, 64, 32};
   const int cands_blk[] = {128, 64, 32};
   const int* c = mode == FP8S_SCALE_BLOCK ? cands_blk : cands_pt;
   const int nc = mode == FP8S_SCALE_BLOCK ? 3 : 4;
+  auto eff = [](int bn) { return bn == 256 ? 1.0 : bn == 128 ? 0.62 : bn == 64 ? 0.40 : 0.25; };
   int best = c[0];
   double best_cost = 1e300;
   for (int i = 0; i < nc; ++i) {
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + c[i] - 1) / c[i]);
     const int64_t waves = (tiles + sms - 1) / sms;
-    const double cost = static_cast<double>(waves) * (c[i] + 32);
+    const double cost = static_cast<double>(waves) * (c[i] / eff(c[i]) + 32);
     if (cost < best_cost) {
       best_cost = cost;
       best = c[i];
@@ -279,14 +307,16 @@ fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int64_t N, i
                                       fp8s_stream_t stream) {
   if (wt != FP8S_F16 && wt != FP8S_BF16) return FP8S_ERR_DTYPE;
   if (!w || !q || !sb) return FP8S_ERR_NULL;
-  if (N < 1 || K < 128 || K % 128 != 0 || K / 128 > 65535 || N > (1LL << 31) - 128) return FP8S_ERR_SHAPE;
+  if (N < 1 || K < 128 || K % 128 != 0 || K / 128 > 65535 || N > (1LL << 31) - 128 ||
+      ((N + 127) / 128) * (K / 128) > (1LL << 31) - 1)
+    return FP8S_ERR_SHAPE;
   if (!aligned16(w) || !aligned16(q) || !aligned16(sb)) return FP8S_ERR_ALIGN;
   int dev;
   DeviceInfo info;
   if (fp8s_status s = current_device(&dev, &info)) return s;
   cudaStream_t st = as_stream(stream);
-  return wt == FP8S_F16 ? launch_weight_block<kInF16>(w, N, K, q, sb, st)
-                        : launch_weight_block<kInBF16>(w, N, K, q, sb, st);
+  return wt == FP8S_F16 ? launch_weight_block<kInF16>(w, N, K, q, sb, st, info, dev)
+                        : launch_weight_block<kInBF16>(w, N, K, q, sb, st, info, dev);
 }
 
 fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, void* c,

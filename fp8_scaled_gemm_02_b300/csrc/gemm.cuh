@@ -31,7 +31,7 @@
 // per-tensor mode, by K blocks in block mode).
 //
 // Every mbarrier wait is bounded in wall time; on expiry the waiting role
-// records where it gave up in g_fp8s_error and leaves its loop; in-flight
+// records where it gave up in g_fp8s_error (quantize.cuh) and leaves its loop; in-flight
 // TMA loads and MMAs are drained (also bounded) before TMEM is freed.
 #pragma once
 
@@ -41,6 +41,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "quantize.cuh"
 
 namespace fp8s {
 
@@ -50,12 +51,6 @@ constexpr int kMmaK = 32;  // K of one tcgen05.mma kind::f8f6f4
 
 enum : int { kModePerTensor = 0, kModeBlock = 1 };
 enum : int { kOutF16 = 0, kOutBF16 = 1 };
-enum : unsigned { kErrProducer = 1, kErrMma = 2, kErrEpilogue = 3 };
-
-// Set by a kernel whose bounded wait expired (first writer wins).
-__device__ unsigned int g_fp8s_error;
-
-__device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_fp8s_error, 0u, code); }
 
 struct GemmParams {
   int M, N, K;
@@ -79,15 +74,29 @@ struct GemmCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kNBuf = (512 / BN) > 4 ? 4 : (512 / BN);
+  // TMEM accumulator buffers: whole tiles (per-tensor) or single K blocks
+  // (block mode; narrow tiles get up to 16 so the MMA can run far ahead).
+  static constexpr int kNBufMax = MODE == kModeBlock ? 16 : 4;
+  static constexpr int kNBuf = (512 / BN) > kNBufMax ? kNBufMax : (512 / BN);
   static constexpr int kTmemCols = kNBuf * BN;
   static constexpr int kColsPerThread = BN / 2;  // per epilogue warpgroup
   static constexpr int kChunk = kColsPerThread < 32 ? kColsPerThread : 32;
+  // Block mode: K blocks the epilogue takes per TMEM hand-off (one
+  // tcgen05.wait::ld per batch), capped by registers and by half the buffers.
+  static constexpr int kBatchRaw = 64 / kColsPerThread;
+  static constexpr int kBatch = MODE == kModeBlock ? (kBatchRaw > kNBuf / 2 ? kNBuf / 2 : kBatchRaw) : 1;
+  static_assert(kBatch >= 1, "batch");
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 1) + 16;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
 };
+
+// First K block of a tile.  Tiles start their K loop at different K blocks
+// so that concurrently running CTAs that share an operand (all CTAs of a
+// decode-sized GEMM share the whole activation) do not all request the same
+// L2 lines at the same time.  Summation order changes per tile, nothing else.
+__device__ __forceinline__ int kb_rotation(int tm, int tn, int num_kb) { return (tm + tn) % num_kb; }
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm, int& tn) {
   const int per_group = p.group_m * p.tiles_n;
@@ -136,6 +145,17 @@ __device__ __forceinline__ void store_row(uint16_t* __restrict__ crow, int n0, i
 #pragma unroll
     for (int j = 0; j < W; ++j)
       if (n0 + j < N) crow[n0 + j] = one_out<OUT>(v[j]);
+  }
+}
+
+// Issues the TMEM load of W columns into r (no wait).
+template <int W>
+__device__ __forceinline__ void tmem_load_nowait(uint32_t taddr, uint32_t* r) {
+  if constexpr (W == 32) {
+    ptx::tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(r));
+  } else {
+    static_assert(W == 16, "chunk width");
+    ptx::tmem_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
   }
 }
 
@@ -212,7 +232,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int tm, tn;
         tile_coords(t, p, tm, tn);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int rot = kb_rotation(tm, tn, p.num_kb);
+        for (int i = 0; i < p.num_kb; ++i) {
+          const int kb = (i + rot) % p.num_kb;
           const int s = issued % S;
           const uint32_t ph = (issued / S) & 1;
           if (!ptx::mbar_wait_bounded(&empty_bar[s], ph ^ 1, p.timeout_ns)) {
@@ -240,7 +262,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
       uint32_t consumed = 0, unit = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        for (int kb = 0; kb < p.num_kb && ok; ++kb) {
+        for (int kb = 0; kb < p.num_kb && ok; ++kb) {  // kb counts K blocks of the tile in issue order
           const bool new_unit = (MODE == kModeBlock) || kb == 0;
           const uint32_t buf = unit % NBUF;
           if (new_unit) {
@@ -323,38 +345,62 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&tempty_bar[buf]);
         ++unit;
       } else {
+        constexpr int KBT = Cfg::kBatch;
         float acc[CPT];
 #pragma unroll
         for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
         const int nb = n_base / 128;  // weight block row of this warpgroup's columns
         const float* sa_col = p.sa + (row < p.M ? row : 0);
         const float* sb_row = p.sb + static_cast<int64_t>(nb) * KB;
-        float sa_next = __ldg(sa_col);
-        float sb_next = __ldg(sb_row);
-        for (int kb = 0; kb < KB; ++kb) {
-          const float sa_v = sa_next, sb_v = sb_next;
-          if (kb + 1 < KB) {
-            sa_next = __ldg(sa_col + static_cast<int64_t>(kb + 1) * p.M);
-            sb_next = __ldg(sb_row + kb + 1);
-          }
-          const uint32_t buf = unit % NBUF;
-          if (!ptx::mbar_wait_bounded(&tfull_bar[buf], (unit / NBUF) & 1, p.timeout_ns)) {
-            record_error(kErrEpilogue);
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          float part[CPT];
+        const int rot = kb_rotation(tm, tn, KB);
+        auto kb_at = [&](int i) { return i + rot < KB ? i + rot : i + rot - KB; };  // i-th K block issued
+        float sa_n[KBT], sb_n[KBT];
 #pragma unroll
-          for (int c = 0; c < CPT / CW; ++c)
-            tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, part + c * CW);
+        for (int j = 0; j < KBT; ++j) {
+          sa_n[j] = j < KB ? __ldg(sa_col + static_cast<int64_t>(kb_at(j)) * p.M) : 0.0f;
+          sb_n[j] = j < KB ? __ldg(sb_row + kb_at(j)) : 0.0f;
+        }
+        for (int kb0 = 0; kb0 < KB; kb0 += KBT) {
+          const int nkb = min(KBT, KB - kb0);
+          float sc[KBT];
+#pragma unroll
+          for (int j = 0; j < KBT; ++j) {
+            sc[j] = sa_n[j] * sb_n[j];
+            const int kn = kb0 + KBT + j;  // prefetch the next batch's scales
+            sa_n[j] = kn < KB ? __ldg(sa_col + static_cast<int64_t>(kb_at(kn)) * p.M) : 0.0f;
+            sb_n[j] = kn < KB ? __ldg(sb_row + kb_at(kn)) : 0.0f;
+          }
+          for (int j = 0; j < nkb && ok; ++j) {
+            const uint32_t u = unit + j;
+            if (!ptx::mbar_wait_bounded(&tfull_bar[u % NBUF], (u / NBUF) & 1, p.timeout_ns)) {
+              record_error(kErrEpilogue);
+              ok = false;
+            }
+          }
+          if (!ok) break;
+          ptx::tc_fence_after();
+          uint32_t part[KBT][CPT];
+#pragma unroll
+          for (int j = 0; j < KBT; ++j) {
+            if (j < nkb) {
+              const uint32_t col0 = ((unit + j) % NBUF) * BN + wg * CPT;
+#pragma unroll
+              for (int c = 0; c < CPT / CW; ++c)
+                tmem_load_nowait<CW>(tmem_base + lane_off + col0 + c * CW, &part[j][c * CW]);
+            }
+          }
+          ptx::tmem_ld_wait();
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&tempty_bar[buf]);
-          ++unit;
-          const float sc = sa_v * sb_v;
+          if (lane == 0)
+            for (int j = 0; j < nkb; ++j) ptx::mbar_arrive(&tempty_bar[(unit + j) % NBUF]);
+          unit += nkb;
 #pragma unroll
-          for (int j = 0; j < CPT; ++j) acc[j] = fmaf(part[j], sc, acc[j]);
+          for (int j = 0; j < KBT; ++j)
+            if (j < nkb) {
+#pragma unroll
+              for (int c = 0; c < CPT; ++c) acc[c] = fmaf(__uint_as_float(part[j][c]), sc[j], acc[c]);
+            }
         }
         if (!ok) break;
         if (row < p.M) {

@@ -18,9 +18,9 @@
 //    q' = q + r*y.  The first refinement leaves q within one ulp of x/s; the
 //    second then returns the correctly rounded quotient (Markstein, "IA-64
 //    and Elementary Functions", theorem on division by reciprocal
-//    refinement).  The result takes the sign of x (x/s with s > 0, which
-//    also keeps -0).  Units whose scale is tiny (s < 2^-90, possible only
-//    for BF16 inputs below about 2^-81) use the IEEE divide __fdiv_rn.
+//    refinement).  Zeros keep the sign of x (x/s with s > 0, so -0 stays
+//    -0).  Units whose scale is tiny (s < 2^-90, possible only for BF16
+//    inputs below about 2^-81) use the IEEE divide __fdiv_rn.
 //  * the E4M3 rounding is the hardware cvt.rn.satfinite.e4m3x2.f32.
 #pragma once
 
@@ -34,6 +34,12 @@
 namespace fp8s {
 
 enum : int { kInF16 = 0, kInBF16 = 1 };
+
+// Device error word shared by every kernel of the library (first writer wins).
+__device__ unsigned int g_fp8s_error;
+enum : unsigned { kErrProducer = 1, kErrMma = 2, kErrEpilogue = 3, kErrQuant = 4 };
+__device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_fp8s_error, 0u, code); }
+__device__ __forceinline__ void record_quant_error() { record_error(kErrQuant); }
 
 // Two packed 16-bit values (low half first) -> two floats.  Exact.
 template <int DT>
@@ -75,32 +81,52 @@ struct UnitScale {
     exact_div = !(s >= 0x1p-90f);
   }
 
-  __device__ __forceinline__ float div(float x) const {
-    if (exact_div) return __fdiv_rn(x, s);
+  // Reciprocal refinement (two Markstein steps); valid when !exact_div.
+  // The remainder is formed negated, r' = s*q - x (exact), and the step is
+  // q - r'*y: for x != 0 this is the same rounding of the same exact value as
+  // q + r*y, and for x = -0 (or a quotient that underflows to zero) the sum
+  // of two like-signed zeros keeps the sign of x, so no copysign is needed.
+  __device__ __forceinline__ float div_fast(float x) const {
     float q = __fmul_rn(x, y);
-    float r = __fmaf_rn(-s, q, x);
-    q = __fmaf_rn(r, y, q);
-    r = __fmaf_rn(-s, q, x);
-    q = __fmaf_rn(r, y, q);
-    return copysignf(q, x);
+    float r = __fmaf_rn(s, q, -x);
+    q = __fmaf_rn(-r, y, q);
+    r = __fmaf_rn(s, q, -x);
+    q = __fmaf_rn(-r, y, q);
+    return q;
+  }
+
+  __device__ __forceinline__ float div_exact(float x) const { return __fdiv_rn(x, s); }
+
+  template <bool kExact>
+  __device__ __forceinline__ float div(float x) const {
+    if constexpr (kExact) return div_exact(x);
+    else return div_fast(x);
   }
 };
 
 // 8 input elements (one 16-byte vector) -> 8 E4M3 bytes.
+template <int DT, bool kExact>
+__device__ __forceinline__ uint2 quant8_impl(const uint4& v, const UnitScale& us) {
+  const float2 a = unpack2<DT>(v.x), b = unpack2<DT>(v.y), c = unpack2<DT>(v.z), d = unpack2<DT>(v.w);
+  const uint32_t p0 = ptx::cvt_e4m3x2(us.div<kExact>(a.y), us.div<kExact>(a.x));
+  const uint32_t p1 = ptx::cvt_e4m3x2(us.div<kExact>(b.y), us.div<kExact>(b.x));
+  const uint32_t p2 = ptx::cvt_e4m3x2(us.div<kExact>(c.y), us.div<kExact>(c.x));
+  const uint32_t p3 = ptx::cvt_e4m3x2(us.div<kExact>(d.y), us.div<kExact>(d.x));
+  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+}
+
+// The per-unit choice of division path is made once, outside the element loop.
 template <int DT>
 __device__ __forceinline__ uint2 quant8(const uint4& v, const UnitScale& us) {
-  const float2 a = unpack2<DT>(v.x), b = unpack2<DT>(v.y), c = unpack2<DT>(v.z), d = unpack2<DT>(v.w);
-  const uint32_t p0 = ptx::cvt_e4m3x2(us.div(a.y), us.div(a.x));
-  const uint32_t p1 = ptx::cvt_e4m3x2(us.div(b.y), us.div(b.x));
-  const uint32_t p2 = ptx::cvt_e4m3x2(us.div(c.y), us.div(c.x));
-  const uint32_t p3 = ptx::cvt_e4m3x2(us.div(d.y), us.div(d.x));
-  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+  if (__builtin_expect(us.exact_div, 0)) return quant8_impl<DT, true>(v, us);
+  return quant8_impl<DT, false>(v, us);
 }
 
 template <int DT>
 __device__ __forceinline__ uint8_t quant1(uint16_t h, const UnitScale& us) {
   float x = unpack2<DT>(static_cast<uint32_t>(h)).x;
-  return static_cast<uint8_t>(ptx::cvt_e4m3x2(0.0f, us.div(x)) & 0xFFu);
+  const float t = us.exact_div ? us.div_exact(x) : us.div_fast(x);
+  return static_cast<uint8_t>(ptx::cvt_e4m3x2(0.0f, t) & 0xFFu);
 }
 
 // Streaming 16-byte load that does not allocate in L1.
@@ -149,42 +175,109 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
 }
 
 // ------------------------------------------------------------------------
-// K4: one 128x128 weight block per CTA of 256 threads.  Thread t holds the
-// 16-byte vectors (row t/16 + 16i, column vector t%16), i = 0..7, so the
-// block is read once and cast from registers.  grid = (ceil(N/128), K/128).
+// K4: persistent CTAs of 8 consumer warps + 1 TMA producer warp.  The
+// producer streams whole 128x128 weight blocks (32 KB of FP16/BF16, one 2-D
+// TMA box each) into a kWbStages-deep shared-memory ring; consumers copy a
+// block into registers (thread t: row t/16 + 16i, 16-byte column t%16,
+// i = 0..7), free the stage at once, reduce the block amax and cast from
+// registers, so loads of the next blocks overlap the cast of this one.
+// Waits are bounded; a consumer that gives up raises a shared abort flag that
+// every consumer reads after the same named barrier, so they leave together.
+constexpr int kWbStages = 3;
+constexpr int kWbBlockBytes = 128 * 128 * 2;
+constexpr int kWbSmemBytes = 1024 + kWbStages * kWbBlockBytes + 256;
+
 template <int DT>
-__global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4* __restrict__ w,
-                                                                 uint2* __restrict__ q,
-                                                                 float* __restrict__ sb, int N, int KB) {
-  __shared__ uint32_t warp_max[8];
-  const int bi = blockIdx.x, bj = blockIdx.y;
+__global__ void __launch_bounds__(288, 2)
+    quant_weight_block_tma_kernel(const __grid_constant__ CUtensorMap tmap_w, uint2* __restrict__ q,
+                                  float* __restrict__ sb, int N, int KB, int num_blocks,
+                                  unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kWbStages * kWbBlockBytes);
+  uint64_t* empty_bar = full_bar + kWbStages;
+  uint32_t* warp_max = reinterpret_cast<uint32_t*>(empty_bar + kWbStages);  // [2][8]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(warp_max + 16);
+
   const int t = threadIdx.x;
-  const int64_t row_vec = static_cast<int64_t>(KB) * 16;
-  const int col = bj * 16 + (t & 15);
-  uint4 v[8];
-  uint32_t a = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = bi * 128 + (t >> 4) + 16 * i;
-    v[i] = make_uint4(0, 0, 0, 0);
-    if (r < N) v[i] = ld_stream(w + r * row_vec + col);
+  const int warp = t >> 5, lane = t & 31;
+  if (t == 0) {
+    for (int s = 0; s < kWbStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 8);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a = max(a, amax_bits8(v[i]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-  if ((t & 31) == 0) warp_max[t >> 5] = a;
   __syncthreads();
-  a = warp_max[0];
+
+  if (warp == 8) {
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmap_w);
+      uint32_t it = 0;
+      for (int b = blockIdx.x; b < num_blocks; b += gridDim.x, ++it) {
+        const int s = it % kWbStages;
+        if (!ptx::mbar_wait_bounded(&empty_bar[s], ((it / kWbStages) & 1) ^ 1, timeout_ns)) {
+          record_quant_error();
+          break;
+        }
+        const int bi = b / KB, bj = b - (b / KB) * KB;
+        ptx::mbar_arrive_expect_tx(&full_bar[s], kWbBlockBytes);
+        ptx::tma_load_2d(smem + s * kWbBlockBytes, &tmap_w, &full_bar[s], bj * 128, bi * 128);
+      }
+      // every issued load lands before the CTA may exit
+      const uint32_t first = it > kWbStages ? it - kWbStages : 0;
+      for (uint32_t j = first; j < it; ++j)
+        if (!ptx::mbar_wait_bounded(&full_bar[j % kWbStages], (j / kWbStages) & 1, timeout_ns)) record_quant_error();
+    }
+  } else {
+    const int64_t row_vec = static_cast<int64_t>(KB) * 16;
+    uint32_t it = 0;
+    for (int b = blockIdx.x; b < num_blocks; b += gridDim.x, ++it) {
+      const int s = it % kWbStages;
+      const int bi = b / KB, bj = b - (b / KB) * KB;
+      const bool ok = ptx::mbar_wait_bounded(&full_bar[s], (it / kWbStages) & 1, timeout_ns);
+      uint4 v[8];
+      uint32_t a = 0;
+      const uint4* tile = reinterpret_cast<const uint4*>(smem + s * kWbBlockBytes);
 #pragma unroll
-  for (int i = 1; i < 8; ++i) a = max(a, warp_max[i]);
-  const UnitScale us(mag_to_float<DT>(a));
+      for (int i = 0; i < 8; ++i) {
+        v[i] = tile[t + 256 * i];
+        a = max(a, amax_bits8(v[i]));
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);
+      if (!ok) {
+        record_quant_error();
+        *abort_flag = 1;
+      }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = bi * 128 + (t >> 4) + 16 * i;
-    if (r < N) q[r * row_vec + col] = quant8<DT>(v[i], us);
+      for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      if (lane == 0) warp_max[(it & 1) * 8 + warp] = a;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (*abort_flag) break;
+      a = warp_max[(it & 1) * 8];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) a = max(a, warp_max[(it & 1) * 8 + i]);
+      const UnitScale us(mag_to_float<DT>(a));
+      const int col = bj * 16 + (t & 15);
+      if (__builtin_expect(!us.exact_div, 1)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = bi * 128 + (t >> 4) + 16 * i;
+          if (r < N) q[r * row_vec + col] = quant8_impl<DT, false>(v[i], us);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = bi * 128 + (t >> 4) + 16 * i;
+          if (r < N) q[r * row_vec + col] = quant8_impl<DT, true>(v[i], us);
+        }
+      }
+      if (t == 0) sb[static_cast<int64_t>(bi) * KB + bj] = us.s;
+    }
   }
-  if (t == 0) sb[static_cast<int64_t>(bi) * KB + bj] = us.s;
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------------

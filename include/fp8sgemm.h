@@ -128,7 +128,8 @@ FP8S_API const char* fp8s_status_string(fp8s_status status);
  * current device's error word, which a kernel sets when one of its bounded
  * waits gives up (the kernel then exits without finishing its output).
  * *where (if not NULL) receives the word: 0 if no wait gave up, else
- * 1 = TMA producer, 2 = MMA issuer, 3 = epilogue.  Returns FP8S_OK,
+ * 1 = GEMM TMA producer, 2 = GEMM MMA issuer, 3 = GEMM epilogue,
+ * 4 = quantizer.  Returns FP8S_OK,
  * FP8S_ERR_DEVICE_TIMEOUT or FP8S_ERR_CUDA.
  */
 FP8S_API fp8s_status fp8s_device_error(fp8s_stream_t stream, int* where);
