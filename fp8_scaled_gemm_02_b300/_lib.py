@@ -31,6 +31,7 @@ SIGNATURES = {
     "fp8s_status_string": (ctypes.c_char_p, [_I]),
     "fp8s_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "fp8s_version": (_I, []),
+    "fp8s_gemm_override": (_I, [_I, _I, _I]),
 }
 
 _lib = None
@@ -48,7 +49,7 @@ def load():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise ImportError(f"{LIB_PATH} is missing: build it with `python -m fp8_scaled_gemm_02_b300.build`")
+            raise ImportError(f"{LIB_PATH} is missing: build it with `python fp8_scaled_gemm_02_b300/build.py`")
         lib = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(lib, name)

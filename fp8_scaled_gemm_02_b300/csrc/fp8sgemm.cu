@@ -166,18 +166,17 @@ fp8s_status ensure_smem_attr(KernelT kern, int bytes, bool* done_per_device) {
 template <int DT>
 fp8s_status launch_token_group(const void* x, int64_t M, int64_t K, uint8_t* q, float* sa, cudaStream_t st,
                                const DeviceInfo& info) {
-  const int G = static_cast<int>(K / 128);
-  const int64_t row_blocks = (M + 15) / 16;
-  const bool big = row_blocks * G >= 16LL * info.sms * 8;
-  if (big) {
-    dim3 grid(static_cast<unsigned>((row_blocks + 3) / 4), G);
-    quant_token_group_kernel<DT, 4><<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), reinterpret_cast<uint2*>(q),
-                                                          sa, static_cast<int>(M), G);
-  } else {
-    dim3 grid(static_cast<unsigned>(row_blocks), G);
-    quant_token_group_kernel<DT, 1><<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), reinterpret_cast<uint2*>(q),
-                                                          sa, static_cast<int>(M), G);
-  }
+  static bool attr_done[kMaxDevices] = {};
+  auto kern = quant_token_group_kernel<DT>;
+  if (fp8s_status s = ensure_smem_attr(kern, kTgSmemBytes, attr_done)) return s;
+  const int64_t G = K / 128;
+  const int64_t groups = M * G;
+  const int64_t chunks = (groups + kTgChunkGroups - 1) / kTgChunkGroups;
+  const int64_t cap = 2LL * info.sms;
+  const unsigned grid = static_cast<unsigned>(chunks < cap ? chunks : cap);
+  kern<<<grid, 288, kTgSmemBytes, st>>>(static_cast<const uint8_t*>(x), reinterpret_cast<uint2*>(q), sa,
+                                         static_cast<uint32_t>(M), static_cast<uint32_t>(G),
+                                         static_cast<uint32_t>(groups), kWaitTimeoutNs);
   return launch_status();
 }
 
@@ -218,52 +217,161 @@ fp8s_status launch_per_tensor(const void* x, int64_t numel, uint8_t* q, float* s
 }
 
 // ------------------------------------------------------------------ GEMM
-template <int BN, int MODE, int OUT>
-fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int sms,
-                            cudaStream_t st) {
-  using Cfg = GemmCfg<BN, MODE>;
-  auto kern = fp8_gemm_kernel<BN, MODE, OUT>;
+struct GemmChoice {
+  int bn = 128;
+  int splits = 1;     // CTAs of a cluster sharing one output tile (split-K)
+  bool pair = false;  // CTA pairs sharing 256 x bn tiles (tcgen05 cta_group::2)
+};
+
+// Tile/split override for tuning sweeps (0 = automatic).
+int g_force_bn = 0;
+int g_force_splits = 0;
+int g_force_pair = 0;
+
+// Most clusters of `splits` CTAs of this kernel the device can hold at once
+// (cached per kernel, cluster size and device).
+template <typename KernelT>
+int max_active_clusters(KernelT kern, int threads, int smem, int splits, int dev, int sms) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, int> cache;
+  const uint64_t key = (reinterpret_cast<uint64_t>(reinterpret_cast<const void*>(kern)) << 8) ^
+                       (static_cast<uint64_t>(splits) << 4) ^ static_cast<uint64_t>(dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(splits * (sms / splits)), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = n;
+  return n;
+}
+
+template <int BN, int MODE, int OUT, bool SPLIT, bool PAIR>
+fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int splits,
+                            const DeviceInfo& info, int dev, cudaStream_t st) {
+  using Cfg = GemmCfg<BN, MODE, SPLIT, PAIR>;
+  auto kern = fp8_gemm_kernel<BN, MODE, OUT, SPLIT, PAIR>;
   static bool attr_set[kMaxDevices] = {};
   if (fp8s_status s = ensure_smem_attr(kern, Cfg::kSmemBytes, attr_set)) return s;
-  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
+  if constexpr (PAIR) {
+    const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, 2, dev, info.sms);
+    if (cmax < 1) return FP8S_ERR_CUDA;
+    const int clusters = p.num_tiles < cmax ? p.num_tiles : cmax;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(Cfg::kThreads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(Cfg::kSmemBytes);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ma, mb, p) != cudaSuccess) return launch_status(), FP8S_ERR_CUDA;
+  } else if constexpr (!SPLIT) {
+    const int grid = p.num_tiles < info.sms ? p.num_tiles : info.sms;
+    kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
+  } else {
+    const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, splits, dev, info.sms);
+    if (cmax < 1) return FP8S_ERR_CUDA;
+    // one tile per cluster: the kernel stages its split-K partials in the
+    // operand ring, which only drains for good after a cluster's last tile
+    if (p.num_tiles > cmax) return FP8S_ERR_SHAPE;
+    const int clusters = p.num_tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * splits), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(Cfg::kThreads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(Cfg::kSmemBytes);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ma, mb, p) != cudaSuccess) return launch_status(), FP8S_ERR_CUDA;
+  }
   return launch_status();
 }
 
-// Tile width: the candidate with the fewest (waves x per-tile cost).  A
-// tile's cost is its width divided by the tensor-pipe efficiency measured for
-// that width on the B300 (narrow tiles are bound by shared-memory operand
-// traffic, not by the MMA), plus a fixed part (pipeline fill, epilogue).
-int choose_bn(int64_t M, int64_t N, int mode, int sms) {
-  const int cands_pt[] = {256, 128, 64, 32};
-  const int cands_blk[] = {128, 64, 32};
-  const int* c = mode == FP8S_SCALE_BLOCK ? cands_blk : cands_pt;
-  const int nc = mode == FP8S_SCALE_BLOCK ? 3 : 4;
-  auto eff = [](int bn) { return bn == 256 ? 1.0 : bn == 128 ? 0.62 : bn == 64 ? 0.40 : 0.25; };
-  int best = c[0];
+// Relative tensor-pipe efficiency of one 128 x BN x 128 K block, measured on
+// the B300 for each tile width (narrow tiles are bound by shared-memory
+// operand traffic, not by the MMA).
+double tile_eff(int bn) { return bn == 256 ? 1.0 : bn == 128 ? 0.62 : bn == 64 ? 0.40 : 0.25; }
+
+// Tile width and split: the candidate with the least estimated time.  A
+// persistent CTA's time is (waves of tiles) x (its K blocks per tile) x (the
+// cost of one K block at that width), plus a fixed part per tile (pipeline
+// fill, epilogue) and, for split-K, the partial exchange.
+GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms) {
+  GemmChoice best;
   double best_cost = 1e300;
-  for (int i = 0; i < nc; ++i) {
-    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + c[i] - 1) / c[i]);
-    const int64_t waves = (tiles + sms - 1) / sms;
-    const double cost = static_cast<double>(waves) * (c[i] / eff(c[i]) + 32);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = c[i];
+  const int bns[] = {256, 128, 64, 32};
+  const int64_t tm = (M + kBM - 1) / kBM;
+  for (int bn : bns) {
+    for (int s = 1; s <= 8; s *= 2) {
+      if (s > KB) continue;
+      const int64_t tiles = tm * ((N + bn - 1) / bn);
+      const int64_t clusters = sms / s;
+      if (s > 1 && tiles > clusters * 7 / 8) continue;  // split-K needs one tile per cluster (with slack for GPC packing)
+      const int64_t waves = (tiles + clusters - 1) / clusters;
+      const int64_t kb = (KB + s - 1) / s;
+      double cost = static_cast<double>(waves) * (static_cast<double>(kb) * bn / tile_eff(bn) + 64.0);
+      if (s > 1) cost += static_cast<double>(waves) * (32.0 + 0.25 * bn * s);
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best.bn = bn;
+        best.splits = s;
+      }
     }
   }
   return best;
 }
 
 template <int MODE, int OUT>
-fp8s_status dispatch_gemm_bn(int bn, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int sms,
-                             cudaStream_t st) {
-  switch (bn) {
-    case 32: return launch_gemm_cfg<32, MODE, OUT>(ma, mb, p, sms, st);
-    case 64: return launch_gemm_cfg<64, MODE, OUT>(ma, mb, p, sms, st);
-    case 128: return launch_gemm_cfg<128, MODE, OUT>(ma, mb, p, sms, st);
-    case 256:
-      if constexpr (MODE == kModePerTensor) return launch_gemm_cfg<256, MODE, OUT>(ma, mb, p, sms, st);
-      return FP8S_ERR_SHAPE;
+fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
+                          const DeviceInfo& info, int dev, cudaStream_t st) {
+  if (ch.pair) {
+    switch (ch.bn) {
+      case 64: return launch_gemm_cfg<64, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+      case 128: return launch_gemm_cfg<128, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+      case 256: return launch_gemm_cfg<256, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+      default: return FP8S_ERR_SHAPE;
+    }
+  }
+  if (ch.splits > 1) {
+    switch (ch.bn) {
+      case 32: return launch_gemm_cfg<32, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
+      case 64: return launch_gemm_cfg<64, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
+      case 128: return launch_gemm_cfg<128, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
+      case 256: return launch_gemm_cfg<256, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
+      default: return FP8S_ERR_SHAPE;
+    }
+  }
+  switch (ch.bn) {
+    case 32: return launch_gemm_cfg<32, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
+    case 64: return launch_gemm_cfg<64, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
+    case 128: return launch_gemm_cfg<128, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
+    case 256: return launch_gemm_cfg<256, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
     default: return FP8S_ERR_SHAPE;
   }
 }
@@ -293,7 +401,8 @@ fp8s_status fp8_quantize_token_group(const void* x, fp8s_dtype xt, int64_t M, in
                                      fp8s_stream_t stream) {
   if (xt != FP8S_F16 && xt != FP8S_BF16) return FP8S_ERR_DTYPE;
   if (!x || !q || !sa) return FP8S_ERR_NULL;
-  if (M < 1 || K < 128 || K % 128 != 0 || K / 128 > 65535 || M > (1LL << 31) - 16) return FP8S_ERR_SHAPE;
+  if (M < 1 || K < 128 || K % 128 != 0 || M > (1LL << 31) - 1 || M * (K / 128) > (1LL << 31) - 1)
+    return FP8S_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sa)) return FP8S_ERR_ALIGN;
   int dev;
   DeviceInfo info;
@@ -335,17 +444,26 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
   if (fp8s_status s = current_device(&dev, &info)) return s;
   cudaStream_t st = as_stream(stream);
 
-  const int bn = choose_bn(M, N, mode, info.sms);
+  const int64_t KB = (K + kBK - 1) / kBK;
+  GemmChoice ch = choose_gemm(M, N, KB, mode, info.sms);
+  if (g_force_bn) {
+    ch.bn = g_force_bn;
+    ch.splits = g_force_splits > 0 ? g_force_splits : 1;
+    ch.pair = g_force_pair != 0;
+    if (ch.splits > KB) return FP8S_ERR_SHAPE;
+  }
+  const int bn = ch.bn;
+  const int tile_m = ch.pair ? 2 * kBM : kBM;
   CUtensorMap ma, mb;
   if (fp8s_status s = tensor_map_e4m3(qa, M, K, kBM, dev, &ma)) return s;
-  if (fp8s_status s = tensor_map_e4m3(qb, N, K, bn, dev, &mb)) return s;
+  if (fp8s_status s = tensor_map_e4m3(qb, N, K, ch.pair ? bn / 2 : bn, dev, &mb)) return s;
 
   GemmParams p;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.num_kb = static_cast<int>((K + kBK - 1) / kBK);
-  p.tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+  p.num_kb = static_cast<int>(KB);
+  p.tiles_m = static_cast<int>((M + tile_m - 1) / tile_m);
   p.tiles_n = static_cast<int>((N + bn - 1) / bn);
   const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (tiles > (1LL << 31) - 1) return FP8S_ERR_SHAPE;
@@ -356,11 +474,36 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
   p.c = c;
   p.timeout_ns = kWaitTimeoutNs;
 
-  if (mode == FP8S_SCALE_PER_TENSOR)
-    return ct == FP8S_F16 ? dispatch_gemm_bn<kModePerTensor, kOutF16>(bn, ma, mb, p, info.sms, st)
-                          : dispatch_gemm_bn<kModePerTensor, kOutBF16>(bn, ma, mb, p, info.sms, st);
-  return ct == FP8S_F16 ? dispatch_gemm_bn<kModeBlock, kOutF16>(bn, ma, mb, p, info.sms, st)
-                        : dispatch_gemm_bn<kModeBlock, kOutBF16>(bn, ma, mb, p, info.sms, st);
+  auto run = [&](const GemmChoice& c) {
+    if (mode == FP8S_SCALE_PER_TENSOR)
+      return ct == FP8S_F16 ? dispatch_gemm<kModePerTensor, kOutF16>(c, ma, mb, p, info, dev, st)
+                            : dispatch_gemm<kModePerTensor, kOutBF16>(c, ma, mb, p, info, dev, st);
+    return ct == FP8S_F16 ? dispatch_gemm<kModeBlock, kOutF16>(c, ma, mb, p, info, dev, st)
+                          : dispatch_gemm<kModeBlock, kOutBF16>(c, ma, mb, p, info, dev, st);
+  };
+  fp8s_status r = run(ch);
+  if (r == FP8S_ERR_SHAPE && ch.splits > 1 && !g_force_bn) {
+    // the device holds fewer clusters than the estimate assumed: no split
+    ch.splits = 1;
+    r = run(ch);
+  }
+  return r;
+}
+
+fp8s_status fp8s_gemm_override(int bn, int splits, int pair) {
+  if (bn == 0) {
+    g_force_bn = 0;
+    g_force_splits = 0;
+    g_force_pair = 0;
+    return FP8S_OK;
+  }
+  if ((bn != 32 && bn != 64 && bn != 128 && bn != 256) || (splits != 1 && splits != 2 && splits != 4 && splits != 8))
+    return FP8S_ERR_SHAPE;
+  if (pair && (splits != 1 || bn < 64)) return FP8S_ERR_SHAPE;
+  g_force_bn = bn;
+  g_force_splits = splits;
+  g_force_pair = pair ? 1 : 0;
+  return FP8S_OK;
 }
 
 const char* fp8s_status_string(fp8s_status status) {

@@ -9,7 +9,7 @@
 // activation-group scale and weight-block scale and added into an FP32
 // accumulator.
 //
-// Design (one CTA per SM, persistent over output tiles of 128 x BN):
+// Design (persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: streams 128x128-byte A tiles and BNx128-byte B
 //               tiles into a STAGES-deep shared-memory ring (128-byte
 //               swizzle), signalling `full` mbarriers by transaction bytes.
@@ -18,9 +18,9 @@
 //               tcgen05.commit frees the smem stage and publishes a TMEM
 //               accumulator buffer.
 //   warp 2      allocates / frees TMEM (NBUF buffers of BN FP32 columns).
-//   warps 4-11  two epilogue warpgroups; warp w reads TMEM lanes
-//               32*(w%4)..+31 (rows of the tile), warpgroup e reads columns
-//               e*BN/2 .. (e+1)*BN/2.
+//   warps 4..   epilogue warpgroups; warp w reads TMEM lanes 32*(w%4)..+31
+//               (rows of the tile), warpgroup e reads columns
+//               e*CPT .. (e+1)*CPT (CPT = BN / number of epilogue warpgroups).
 //     per-tensor: the accumulator of a whole tile stays in TMEM; the
 //               epilogue loads it once, multiplies by sA*sB, rounds and stores.
 //     block:    every K block lands in its own TMEM buffer (the MMA starts a
@@ -30,9 +30,30 @@
 // NBUF TMEM buffers let the MMA run ahead of the epilogue (by whole tiles in
 // per-tensor mode, by K blocks in block mode).
 //
+// Split-K over a thread-block cluster (SPLIT = true, for shapes with too few
+// output tiles to occupy the GPU): the S CTAs of a cluster share one output
+// tile and CTA rank r takes K blocks [r*KB/S, (r+1)*KB/S).  Every cluster
+// owns exactly one tile, so once its last MMA has retired the operand ring is
+// idle and doubles as the staging buffer: each CTA leaves its FP32 partial
+// tile (already rescaled) there, 128 columns per pass; after a cluster-wide
+// mbarrier hand-off, rank r sums rows [r*128/S, (r+1)*128/S) of all S
+// partials in rank order (distributed shared memory loads), rounds and
+// stores them.  The summation order is fixed, so results are deterministic,
+// and no global scratch memory is used.
+//
+// CTA pairs (PAIR = true, large shapes): the two CTAs of a cluster share an
+// output tile of 256 x BN.  Each loads its own 128 rows of A and half (BN/2
+// rows) of B per K block; the leader (even rank) issues tcgen05.mma
+// .cta_group::2 with M = 256, which reads both CTAs' shared memory and writes
+// each CTA's 128 rows into its own TMEM, and multicasts its commits to both
+// CTAs.  Per CTA this halves the B operand traffic of a 128 x BN tile, so a
+// 256 x 128 pair tile feeds the tensor core like a 128 x 256 single-CTA tile
+// while each epilogue keeps a 128 x 128 accumulator.
+//
 // Every mbarrier wait is bounded in wall time; on expiry the waiting role
-// records where it gave up in g_fp8s_error (quantize.cuh) and leaves its loop; in-flight
-// TMA loads and MMAs are drained (also bounded) before TMEM is freed.
+// records where it gave up in g_fp8s_error (quantize.cuh) and leaves its
+// loop; in-flight TMA loads and MMAs are drained (also bounded) before TMEM is
+// freed, and CTAs of a cluster leave together through one cluster barrier.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -63,40 +84,60 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool SPLIT, bool PAIR = false>
 struct GemmCfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN");
-  static_assert(MODE == kModePerTensor || BN <= 128, "block mode keeps BN/2 accumulators per thread");
-  static constexpr int kEpiWarps = 8;
-  static constexpr int kThreads = 128 + 32 * kEpiWarps;
+  static_assert(!(SPLIT && PAIR), "a CTA pair does not also split K");
+  static_assert(!PAIR || BN >= 64, "a CTA pair holds at least 32 rows of B each");
+  // Block mode keeps 64 FP32 accumulators per epilogue thread: BN = 256
+  // needs four epilogue warpgroups.
+  static constexpr int kEpiWarps = (MODE == kModeBlock && BN == 256) ? 16 : 8;
+  static constexpr int kEpiWG = kEpiWarps / 4;
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kThreads = 128 + kEpiThreads;
+  static constexpr bool kLowReg = kEpiWarps == 16;  // 640 threads: at most 96 registers each
+  static constexpr int kTileM = PAIR ? 2 * kBM : kBM;   // output rows per (pair) tile
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;     // rows of B this CTA loads
   static constexpr int kABytes = kBM * kBK;
-  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kBBytes = kBRows * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  // Split-K partial: exchanged in passes of up to 128 columns (128 rows x
+  // 128 FP32 = 64 KB of shared memory), rows padded by 4 words so that
+  // 16-byte writes of 8 consecutive rows cover all 32 banks.
+  static constexpr int kPassCols = BN < 128 ? BN : 128;
+  static constexpr int kPasses = BN / kPassCols;
+  static constexpr int kStagePitch = kPassCols + 4;
+  static constexpr int kStagingBytes = kBM * kStagePitch * 4;  // aliases the operand ring
+  static constexpr int kStagesRaw = (210 * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(!SPLIT || kStages * kStageBytes >= kStagingBytes, "staging fits in the ring");
   // TMEM accumulator buffers: whole tiles (per-tensor) or single K blocks
   // (block mode; narrow tiles get up to 16 so the MMA can run far ahead).
   static constexpr int kNBufMax = MODE == kModeBlock ? 16 : 4;
-  static constexpr int kNBuf = (512 / BN) > kNBufMax ? kNBufMax : (512 / BN);
+  static constexpr int kTmemMax = PAIR ? 256 : 512;
+  static constexpr int kNBuf = (kTmemMax / BN) > kNBufMax ? kNBufMax : (kTmemMax / BN);
   static constexpr int kTmemCols = kNBuf * BN;
-  static constexpr int kColsPerThread = BN / 2;  // per epilogue warpgroup
-  static constexpr int kChunk = kColsPerThread < 32 ? kColsPerThread : 32;
+  static constexpr int kColsPerThread = BN / kEpiWG;
+  static constexpr int kChunk = kLowReg ? 16 : (kColsPerThread < 32 ? kColsPerThread : 32);
   // Block mode: K blocks the epilogue takes per TMEM hand-off (one
   // tcgen05.wait::ld per batch), capped by registers and by half the buffers.
   static constexpr int kBatchRaw = 64 / kColsPerThread;
-  static constexpr int kBatch = MODE == kModeBlock ? (kBatchRaw > kNBuf / 2 ? kNBuf / 2 : kBatchRaw) : 1;
+  static constexpr int kBatch =
+      (MODE == kModeBlock && !kLowReg) ? (kBatchRaw > kNBuf / 2 ? kNBuf / 2 : kBatchRaw) : 1;
   static_assert(kBatch >= 1, "batch");
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 1) + 16;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 1 + 2) + 16;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
 };
 
-// First K block of a tile.  Tiles start their K loop at different K blocks
-// so that concurrently running CTAs that share an operand (all CTAs of a
-// decode-sized GEMM share the whole activation) do not all request the same
-// L2 lines at the same time.  Summation order changes per tile, nothing else.
-__device__ __forceinline__ int kb_rotation(int tm, int tn, int num_kb) { return (tm + tn) % num_kb; }
+// First K block (within the CTA's K range) of a tile.  Tiles start their K
+// loop at different K blocks so that concurrently running CTAs that share an
+// operand (all CTAs of a decode-sized GEMM share the whole activation) do not
+// all request the same L2 lines at the same time.  Summation order changes
+// per tile, nothing else.
+__device__ __forceinline__ int kb_rotation(int tm, int tn, int nkb) { return (tm + tn) % nkb; }
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm, int& tn) {
   const int per_group = p.group_m * p.tiles_n;
@@ -161,28 +202,104 @@ __device__ __forceinline__ void tmem_load_nowait(uint32_t taddr, uint32_t* r) {
 
 template <int W>
 __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* out) {
-  if constexpr (W == 32) {
-    uint32_t r[32];
-    ptx::tmem_ld_32x32b_x32(taddr, r);
-    ptx::tmem_ld_wait();
+  uint32_t r[W];
+  tmem_load_nowait<W>(taddr, r);
+  ptx::tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(r[j]);
-  } else {
-    static_assert(W == 16, "chunk width");
-    uint32_t r[16];
-    ptx::tmem_ld_32x32b_x16(taddr, r);
-    ptx::tmem_ld_wait();
+  for (int j = 0; j < W; ++j) out[j] = __uint_as_float(r[j]);
+}
+
+// acc[0..1] += {p0, p1} * sc: one packed FMA for two accumulators (each half
+// rounds exactly like fmaf).
+__device__ __forceinline__ void promote2(float* acc, uint32_t p0, uint32_t p1, float sc) {
+  const uint64_t r = ptx::f2_fma(ptx::f2_pack(__uint_as_float(p0), __uint_as_float(p1)), ptx::f2_pack(sc, sc),
+                                 ptx::f2_pack(acc[0], acc[1]));
+  ptx::f2_unpack(r, acc[0], acc[1]);
+}
+
+// Writes W consecutive FP32 values of one staging row (16-byte stores).
+template <int W>
+__device__ __forceinline__ void stage_row(float* srow, const float* v) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) out[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < W; j += 4) *reinterpret_cast<float4*>(srow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+}
+
+// Split-K reduction: this CTA's rows of one column pass (columns col0 ..
+// col0 + PASS_COLS of the tile), summed over the S partials of the cluster
+// in rank order, rounded and stored.  `tid` indexes the epilogue threads.
+template <int BN, int PASS_COLS, int OUT>
+__device__ __forceinline__ void reduce_partials(uint32_t staging_addr, uint32_t rank, uint32_t S, int tid,
+                                                int nthreads, int tm, int tn, int col0, const GemmParams& p) {
+  constexpr int kPitch = PASS_COLS + 4;
+  constexpr int kVecPerRow = PASS_COLS / 4;
+  const int rows = kBM / static_cast<int>(S);
+  const int row0 = static_cast<int>(rank) * rows;
+  uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
+  const bool vec_ok = (p.N % 4) == 0;
+  for (int v = tid; v < rows * kVecPerRow; v += nthreads) {
+    const int r = row0 + v / kVecPerRow;
+    const int c4 = (v % kVecPerRow) * 4;
+    const uint32_t off = staging_addr + static_cast<uint32_t>((r * kPitch + c4) * 4);
+    float4 acc = ptx::ld_dsmem_f4(ptx::mapa(off, 0));
+    for (uint32_t q = 1; q < S; ++q) {
+      const float4 t = ptx::ld_dsmem_f4(ptx::mapa(off, q));
+      acc.x += t.x;
+      acc.y += t.y;
+      acc.z += t.z;
+      acc.w += t.w;
+    }
+    const int row = tm * kBM + r;
+    const int n = tn * BN + col0 + c4;
+    if (row >= p.M) continue;
+    uint16_t* crow = C + static_cast<int64_t>(row) * p.N;
+    if (vec_ok && n + 4 <= p.N) {
+      uint2 pk;
+      pk.x = pack_out<OUT>(acc.x, acc.y);
+      pk.y = pack_out<OUT>(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(crow + n) = pk;
+    } else {
+      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (n + j < p.N) crow[n + j] = one_out<OUT>(a4[j]);
+    }
   }
 }
 
-template <int BN, int MODE, int OUT>
-__global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
+// Tells the MMA issuer a TMEM accumulator buffer has been read.  In a CTA
+// pair the issuer (and the barrier) lives in the leader CTA.
+template <bool PAIR>
+__device__ __forceinline__ void release_tmem(uint64_t* bar) {
+  if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(bar), 0));
+  else ptx::mbar_arrive(bar);
+}
+
+// Split-K hand-off of one column pass: publish this CTA's staged partial to
+// every CTA of the cluster, wait until all S partials are staged, reduce this
+// CTA's rows, then tell every CTA that its partial has been read.  Returns
+// false (after recording the error) if the wait gave up.
+template <int BN, int OUT>
+__device__ __forceinline__ bool exchange_and_reduce(uint64_t* ready_bar, uint64_t* done_bar, uint32_t staging_addr,
+                                                    uint32_t rank, uint32_t S, int tid, int nthreads, int tm, int tn,
+                                                    int pass, uint32_t it, const GemmParams& p) {
+  constexpr int kPassCols = BN < 128 ? BN : 128;
+  for (uint32_t q = 0; q < S; ++q) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(ready_bar), q));
+  if (!ptx::mbar_wait_cluster_bounded(ready_bar, it & 1, p.timeout_ns)) {
+    record_error(kErrEpilogue);
+    return false;
+  }
+  reduce_partials<BN, kPassCols, OUT>(staging_addr, rank, S, tid, nthreads, tm, tn, pass * kPassCols, p);
+  for (uint32_t q = 0; q < S; ++q) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(done_bar), q));
+  return true;
+}
+
+template <int BN, int MODE, int OUT, bool SPLIT, bool PAIR>
+__global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmParams p) {
-  using Cfg = GemmCfg<BN, MODE>;
-  constexpr int S = Cfg::kStages;
+  using Cfg = GemmCfg<BN, MODE, SPLIT, PAIR>;
+  constexpr int TM = Cfg::kTileM;
+  constexpr int S_ = Cfg::kStages;
   constexpr int NBUF = Cfg::kNBuf;
   constexpr int CPT = Cfg::kColsPerThread;
   constexpr int CW = Cfg::kChunk;
@@ -190,91 +307,154 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;
-  uint8_t* smem_b = smem + S * Cfg::kABytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + S * Cfg::kBBytes);
-  uint64_t* empty_bar = full_bar + S;
-  uint64_t* tfull_bar = empty_bar + S;
+  uint8_t* smem_b = smem + S_ * Cfg::kABytes;
+  float* staging = reinterpret_cast<float*>(smem);  // split-K only: used after the ring has drained
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + S_ * Cfg::kBBytes);
+  uint64_t* empty_bar = full_bar + S_;
+  uint64_t* tfull_bar = empty_bar + S_;
   uint64_t* tempty_bar = tfull_bar + NBUF;
   uint64_t* mma_done_bar = tempty_bar + NBUF;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done_bar + 1);
+  uint64_t* ready_bar = mma_done_bar + 1;  // split-K: all S partials of the tile are staged
+  uint64_t* done_bar = ready_bar + 1;      // split-K: all S CTAs finished reading this CTA's partial
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile uint32_t* pair_bad = tmem_slot + 1;  // CTA pair: the two TMEM allocations disagree
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // Work split: without split-K every CTA is its own "cluster" of one; a CTA
+  // pair is a cluster of two sharing one tile and the whole K range.
+  uint32_t rank = 0, S = 1, prank = 0;
+  if constexpr (SPLIT) {
+    rank = ptx::cluster_ctarank();
+    S = ptx::cluster_nctarank();
+  }
+  if constexpr (PAIR) prank = ptx::cluster_ctarank();
+  const bool leader = prank == 0;
+  const int csize = PAIR ? 2 : static_cast<int>(S);
+  const int cluster_id = static_cast<int>(blockIdx.x / csize);
+  const int num_clusters = static_cast<int>(gridDim.x / csize);
+  const int kb_begin = static_cast<int>((static_cast<int64_t>(rank) * p.num_kb) / S);
+  const int kb_end = static_cast<int>((static_cast<int64_t>(rank + 1) * p.num_kb) / S);
+  const int nkb = kb_end - kb_begin;  // >= 1: the host keeps S <= num_kb
+  // Split-K reuses the operand ring as staging, which is only safe when every
+  // cluster owns a single tile; the host guarantees it, this is a backstop.
+  if (SPLIT && num_clusters < p.num_tiles) {
+    if (threadIdx.x == 0 && rank == 0) record_error(kErrProducer);
+    return;
+  }
+
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmap_a);
     ptx::tma_prefetch_desc(&tmap_b);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < S_; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < NBUF; ++b) {
       ptx::mbar_init(&tfull_bar[b], 1);
-      ptx::mbar_init(&tempty_bar[b], Cfg::kEpiWarps);
+      ptx::mbar_init(&tempty_bar[b], (PAIR ? 2 : 1) * Cfg::kEpiWarps);
     }
     ptx::mbar_init(mma_done_bar, 1);
+    ptx::mbar_init(ready_bar, S * Cfg::kEpiThreads);
+    ptx::mbar_init(done_bar, S * Cfg::kEpiThreads);
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
-    ptx::tmem_alloc<Cfg::kTmemCols>(tmem_slot);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair<Cfg::kTmemCols>(tmem_slot);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc<Cfg::kTmemCols>(tmem_slot);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (SPLIT || PAIR) ptx::cluster_sync_all();  // peers' barriers are initialised before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if constexpr (PAIR) {
+    // The pair's MMAs write the leader's TMEM address in both CTAs; make sure
+    // both allocations returned it (both CTAs see the same answer).
+    if (threadIdx.x == 0) {
+      const uint32_t other = ptx::ld_dsmem_u32(ptx::mapa(ptx::smem_u32(tmem_slot), prank ^ 1));
+      *pair_bad = other != tmem_base ? 1u : 0u;
+      if (other != tmem_base) record_error(kErrMma);
+    }
+    __syncthreads();
+  }
+  const bool run_roles = !(PAIR && *pair_bad);
 
-  if (warp == 0) {
+  if (!run_roles) {
+    // nothing: the CTA pair could not share its accumulators
+  } else if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint32_t full0 = PAIR ? ptx::mapa(ptx::smem_u32(full_bar), 0) : ptx::smem_u32(full_bar);
       uint32_t issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
         int tm, tn;
         tile_coords(t, p, tm, tn);
-        const int rot = kb_rotation(tm, tn, p.num_kb);
-        for (int i = 0; i < p.num_kb; ++i) {
-          const int kb = (i + rot) % p.num_kb;
-          const int s = issued % S;
-          const uint32_t ph = (issued / S) & 1;
+        const int rot = kb_rotation(tm, tn, nkb);
+        for (int i = 0; i < nkb; ++i) {
+          const int kb = kb_begin + (i + rot < nkb ? i + rot : i + rot - nkb);
+          const int s = issued % S_;
+          const uint32_t ph = (issued / S_) & 1;
           if (!ptx::mbar_wait_bounded(&empty_bar[s], ph ^ 1, p.timeout_ns)) {
             record_error(kErrProducer);
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kStageBytes);
-          ptx::tma_load_2d(smem_a + s * Cfg::kABytes, &tmap_a, &full_bar[s], kb * kBK, tm * kBM);
-          ptx::tma_load_2d(smem_b + s * Cfg::kBBytes, &tmap_b, &full_bar[s], kb * kBK, tn * BN);
+          if constexpr (PAIR) {
+            // both CTAs' loads count on the leader's barrier
+            if (leader) ptx::mbar_arrive_expect_tx(&full_bar[s], 2 * Cfg::kStageBytes);
+            const uint32_t fb = full0 + 8u * static_cast<uint32_t>(s);
+            ptx::tma_load_2d_pair(smem_a + s * Cfg::kABytes, &tmap_a, fb, kb * kBK, tm * TM + prank * kBM);
+            ptx::tma_load_2d_pair(smem_b + s * Cfg::kBBytes, &tmap_b, fb, kb * kBK, tn * BN + prank * (BN / 2));
+          } else {
+            ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kStageBytes);
+            ptx::tma_load_2d(smem_a + s * Cfg::kABytes, &tmap_a, &full_bar[s], kb * kBK, tm * kBM);
+            ptx::tma_load_2d(smem_b + s * Cfg::kBBytes, &tmap_b, &full_bar[s], kb * kBK, tn * BN);
+          }
           ++issued;
         }
       }
-      // Drain: every issued load has landed before the CTA may exit.
-      const uint32_t first = issued > S ? issued - S : 0;
-      for (uint32_t j = first; j < issued; ++j)
-        if (!ptx::mbar_wait_bounded(&full_bar[j % S], (j / S) & 1, p.timeout_ns)) record_error(kErrProducer);
+      // Drain: every issued load has landed before the CTA may exit.  A pair
+      // member waits until the MMA has consumed (and released) its last
+      // stages, which also means the leader's multicast arrivals have landed.
+      const uint32_t first = issued > S_ ? issued - S_ : 0;
+      for (uint32_t j = first; j < issued; ++j) {
+        const bool done = PAIR ? ptx::mbar_wait_bounded(&empty_bar[j % S_], (j / S_) & 1, p.timeout_ns)
+                               : ptx::mbar_wait_bounded(&full_bar[j % S_], (j / S_) & 1, p.timeout_ns);
+        if (!done) record_error(kErrProducer);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = ptx::idesc_e4m3_f32(TM, BN);
       const uint32_t a0 = ptx::smem_u32(smem_a);
       const uint32_t b0 = ptx::smem_u32(smem_b);
       uint32_t consumed = 0, unit = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        for (int kb = 0; kb < p.num_kb && ok; ++kb) {  // kb counts K blocks of the tile in issue order
-          const bool new_unit = (MODE == kModeBlock) || kb == 0;
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        for (int i = 0; i < nkb && ok; ++i) {  // i counts K blocks of the tile in issue order
+          const bool new_unit = (MODE == kModeBlock) || i == 0;
           const uint32_t buf = unit % NBUF;
           if (new_unit) {
-            if (!ptx::mbar_wait_bounded(&tempty_bar[buf], ((unit / NBUF) & 1) ^ 1, p.timeout_ns)) {
+            const bool freed = PAIR ? ptx::mbar_wait_cluster_bounded(&tempty_bar[buf], ((unit / NBUF) & 1) ^ 1, p.timeout_ns)
+                                    : ptx::mbar_wait_bounded(&tempty_bar[buf], ((unit / NBUF) & 1) ^ 1, p.timeout_ns);
+            if (!freed) {
               record_error(kErrMma);
               ok = false;
               break;
             }
             ptx::tc_fence_after();
           }
-          const int s = consumed % S;
-          if (!ptx::mbar_wait_bounded(&full_bar[s], (consumed / S) & 1, p.timeout_ns)) {
+          const int s = consumed % S_;
+          if (!ptx::mbar_wait_bounded(&full_bar[s], (consumed / S_) & 1, p.timeout_ns)) {
             record_error(kErrMma);
             ok = false;
             break;
@@ -286,41 +466,52 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / kMmaK; ++k) {
             // advance 32 bytes (2 x 16-byte units) along K inside the swizzled row
-            const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (kb > 0 || k > 0);
-            ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
+            const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (i > 0 || k > 0);
+            if constexpr (PAIR) ptx::mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
+            else ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
           }
-          ptx::mma_commit(&empty_bar[s]);
+          if constexpr (PAIR) ptx::mma_commit_pair_mc(&empty_bar[s], 0x3);
+          else ptx::mma_commit(&empty_bar[s]);
           ++consumed;
-          const bool unit_done = (MODE == kModeBlock) || kb == p.num_kb - 1;
+          const bool unit_done = (MODE == kModeBlock) || i == nkb - 1;
           if (unit_done) {
-            ptx::mma_commit(&tfull_bar[buf]);
+            if constexpr (PAIR) ptx::mma_commit_pair_mc(&tfull_bar[buf], 0x3);
+            else ptx::mma_commit(&tfull_bar[buf]);
             ++unit;
           }
         }
       }
       // Drain: all issued MMAs complete before TMEM can be released.
-      ptx::mma_commit(mma_done_bar);
+      if constexpr (PAIR) ptx::mma_commit_pair_mc(mma_done_bar, 0x1);
+      else ptx::mma_commit(mma_done_bar);
       if (!ptx::mbar_wait_bounded(mma_done_bar, 0, p.timeout_ns)) record_error(kErrMma);
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------------- epilogue
+    const int epi_tid = threadIdx.x - 128;
     const int epi_warp = warp - 4;
     const int quarter = warp & 3;   // TMEM lane quarter this warp may access
-    const int wg = epi_warp >> 2;   // column half of the tile
+    const int wg = epi_warp >> 2;   // column slice of the tile
+    const int row_local = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const bool vec_ok = (p.N % 8) == 0;
     uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
-    const int KB = p.num_kb;
+    // split-K: this thread's columns go to staging pass wg*CPT / kPassCols
+    constexpr int kPassCols = Cfg::kPassCols;
+    const int my_pass = (wg * CPT) / kPassCols;
+    float* srow = staging + row_local * Cfg::kStagePitch + (wg * CPT - my_pass * kPassCols);
+    const uint32_t staging_addr = ptx::smem_u32(staging);
     uint32_t unit = 0;
+    uint32_t it = 0;  // tiles this CTA has finished (split-K barrier phases)
     bool ok = true;
 
     float pt_scale = 0.0f;
     if constexpr (MODE == kModePerTensor) pt_scale = __ldg(p.sa) * __ldg(p.sb);
 
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
       int tm, tn;
       tile_coords(t, p, tm, tn);
-      const int row = tm * kBM + quarter * 32 + lane;
+      const int row = tm * TM + static_cast<int>(prank) * kBM + row_local;
       const int n_base = tn * BN + wg * CPT;
       uint16_t* crow = C + static_cast<int64_t>(row) * p.N;
 
@@ -332,18 +523,45 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
+        if constexpr (SPLIT) {
+          for (int h = 0; h < Cfg::kPasses && ok; ++h) {
+            if (it > 0 && !ptx::mbar_wait_cluster_bounded(done_bar, (it - 1) & 1, p.timeout_ns)) {
+              record_error(kErrEpilogue);
+              ok = false;
+              break;
+            }
+            if (my_pass == h) {
 #pragma unroll
-        for (int c = 0; c < CPT / CW; ++c) {
-          float v[CW];
-          tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
+              for (int c = 0; c < CPT / CW; ++c) {
+                float v[CW];
+                tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
 #pragma unroll
-          for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
-          if (row < p.M) store_row<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, v);
+                for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
+                stage_row<CW>(srow + c * CW, v);
+              }
+            }
+            if (!exchange_and_reduce<BN, OUT>(ready_bar, done_bar, staging_addr, rank, S, epi_tid,
+                                              Cfg::kEpiThreads, tm, tn, h, it, p)) {
+              ok = false;
+              break;
+            }
+            ++it;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < CPT / CW; ++c) {
+            float v[CW];
+            tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
+#pragma unroll
+            for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
+            if (row < p.M) store_row<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, v);
+          }
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&tempty_bar[buf]);
+        if (lane == 0) release_tmem<PAIR>(&tempty_bar[buf]);
         ++unit;
+        if (!ok) break;
       } else {
         constexpr int KBT = Cfg::kBatch;
         float acc[CPT];
@@ -351,26 +569,27 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
         for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
         const int nb = n_base / 128;  // weight block row of this warpgroup's columns
         const float* sa_col = p.sa + (row < p.M ? row : 0);
-        const float* sb_row = p.sb + static_cast<int64_t>(nb) * KB;
-        const int rot = kb_rotation(tm, tn, KB);
-        auto kb_at = [&](int i) { return i + rot < KB ? i + rot : i + rot - KB; };  // i-th K block issued
+        const float* sb_row = p.sb + static_cast<int64_t>(nb) * p.num_kb;
+        const int rot = kb_rotation(tm, tn, nkb);
+        // global K block of the i-th K block issued for this tile
+        auto kb_at = [&](int i) { return kb_begin + (i + rot < nkb ? i + rot : i + rot - nkb); };
         float sa_n[KBT], sb_n[KBT];
 #pragma unroll
         for (int j = 0; j < KBT; ++j) {
-          sa_n[j] = j < KB ? __ldg(sa_col + static_cast<int64_t>(kb_at(j)) * p.M) : 0.0f;
-          sb_n[j] = j < KB ? __ldg(sb_row + kb_at(j)) : 0.0f;
+          sa_n[j] = j < nkb ? __ldg(sa_col + static_cast<int64_t>(kb_at(j)) * p.M) : 0.0f;
+          sb_n[j] = j < nkb ? __ldg(sb_row + kb_at(j)) : 0.0f;
         }
-        for (int kb0 = 0; kb0 < KB; kb0 += KBT) {
-          const int nkb = min(KBT, KB - kb0);
+        for (int kb0 = 0; kb0 < nkb; kb0 += KBT) {
+          const int nbat = min(KBT, nkb - kb0);
           float sc[KBT];
 #pragma unroll
           for (int j = 0; j < KBT; ++j) {
             sc[j] = sa_n[j] * sb_n[j];
             const int kn = kb0 + KBT + j;  // prefetch the next batch's scales
-            sa_n[j] = kn < KB ? __ldg(sa_col + static_cast<int64_t>(kb_at(kn)) * p.M) : 0.0f;
-            sb_n[j] = kn < KB ? __ldg(sb_row + kb_at(kn)) : 0.0f;
+            sa_n[j] = kn < nkb ? __ldg(sa_col + static_cast<int64_t>(kb_at(kn)) * p.M) : 0.0f;
+            sb_n[j] = kn < nkb ? __ldg(sb_row + kb_at(kn)) : 0.0f;
           }
-          for (int j = 0; j < nkb && ok; ++j) {
+          for (int j = 0; j < nbat && ok; ++j) {
             const uint32_t u = unit + j;
             if (!ptx::mbar_wait_bounded(&tfull_bar[u % NBUF], (u / NBUF) & 1, p.timeout_ns)) {
               record_error(kErrEpilogue);
@@ -379,44 +598,92 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE>::kThreads, 1)
           }
           if (!ok) break;
           ptx::tc_fence_after();
-          uint32_t part[KBT][CPT];
+          if constexpr (Cfg::kLowReg) {
+            // One K block at a time, 16 columns per TMEM load: 64
+            // accumulators + 16 staged values fit the 96-register budget.
+            const uint32_t col0 = (unit % NBUF) * BN + wg * CPT;
 #pragma unroll
-          for (int j = 0; j < KBT; ++j) {
-            if (j < nkb) {
-              const uint32_t col0 = ((unit + j) % NBUF) * BN + wg * CPT;
+            for (int c = 0; c < CPT / CW; ++c) {
+              uint32_t part[CW];
+              tmem_load_nowait<CW>(tmem_base + lane_off + col0 + c * CW, part);
+              ptx::tmem_ld_wait();
+              if (c == CPT / CW - 1) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_tmem<PAIR>(&tempty_bar[unit % NBUF]);
+              }
 #pragma unroll
-              for (int c = 0; c < CPT / CW; ++c)
-                tmem_load_nowait<CW>(tmem_base + lane_off + col0 + c * CW, &part[j][c * CW]);
+              for (int j = 0; j < CW; j += 2) promote2(&acc[c * CW + j], part[j], part[j + 1], sc[0]);
             }
+            unit += 1;
+          } else {
+            uint32_t part[KBT][CPT];
+#pragma unroll
+            for (int j = 0; j < KBT; ++j) {
+              if (j < nbat) {
+                const uint32_t col0 = ((unit + j) % NBUF) * BN + wg * CPT;
+#pragma unroll
+                for (int c = 0; c < CPT / CW; ++c)
+                  tmem_load_nowait<CW>(tmem_base + lane_off + col0 + c * CW, &part[j][c * CW]);
+              }
+            }
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+              for (int j = 0; j < nbat; ++j) release_tmem<PAIR>(&tempty_bar[(unit + j) % NBUF]);
+            unit += nbat;
+#pragma unroll
+            for (int j = 0; j < KBT; ++j)
+              if (j < nbat) {
+#pragma unroll
+                for (int c = 0; c < CPT; c += 2) promote2(&acc[c], part[j][c], part[j][c + 1], sc[j]);
+              }
           }
-          ptx::tmem_ld_wait();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0)
-            for (int j = 0; j < nkb; ++j) ptx::mbar_arrive(&tempty_bar[(unit + j) % NBUF]);
-          unit += nkb;
-#pragma unroll
-          for (int j = 0; j < KBT; ++j)
-            if (j < nkb) {
-#pragma unroll
-              for (int c = 0; c < CPT; ++c) acc[c] = fmaf(__uint_as_float(part[j][c]), sc[j], acc[c]);
-            }
         }
         if (!ok) break;
-        if (row < p.M) {
+        if constexpr (SPLIT) {
+          for (int h = 0; h < Cfg::kPasses && ok; ++h) {
+            if (it > 0 && !ptx::mbar_wait_cluster_bounded(done_bar, (it - 1) & 1, p.timeout_ns)) {
+              record_error(kErrEpilogue);
+              ok = false;
+              break;
+            }
+            if (my_pass == h) stage_row<CPT>(srow, acc);
+            if (!exchange_and_reduce<BN, OUT>(ready_bar, done_bar, staging_addr, rank, S, epi_tid,
+                                              Cfg::kEpiThreads, tm, tn, h, it, p)) {
+              ok = false;
+              break;
+            }
+            ++it;
+          }
+          if (!ok) break;
+        } else {
+          if (row < p.M) {
 #pragma unroll
-          for (int c = 0; c < CPT / CW; ++c) store_row<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, acc + c * CW);
+            for (int c = 0; c < CPT / CW; ++c) store_row<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, acc + c * CW);
+          }
         }
       }
+
+    }
+    if constexpr (SPLIT) {
+      // Nobody may still be reading this CTA's partial when it exits.
+      if (ok && it > 0 && !ptx::mbar_wait_cluster_bounded(done_bar, (it - 1) & 1, p.timeout_ns))
+        record_error(kErrEpilogue);
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  // A pair frees its TMEM together, after both CTAs are done with it.
+  if constexpr (PAIR) ptx::cluster_sync_all();
   if (warp == 2) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc<Cfg::kTmemCols>(tmem_base);
+    if constexpr (PAIR) ptx::tmem_dealloc_pair<Cfg::kTmemCols>(tmem_base);
+    else ptx::tmem_dealloc<Cfg::kTmemCols>(tmem_base);
   }
+  if constexpr (SPLIT || PAIR) ptx::cluster_sync_all();  // no CTA leaves while a peer may touch its shared memory
 }
 
 }  // namespace fp8s

@@ -15,7 +15,7 @@
 //  * fl32(x / s) is computed without a per-element divide.  With y the
 //    correctly rounded reciprocal of s (computed once per unit), q0 = x*y is
 //    refined twice by the remainder r = x - s*q (exact via FMA) and
-//    q' = q + r*y.  The first refinement leaves q within one ulp of x/s; the
+//    q' = q + r*y (two elements at a time with the packed .f32x2 FMA).  The first refinement leaves q within one ulp of x/s; the
 //    second then returns the correctly rounded quotient (Markstein, "IA-64
 //    and Elementary Functions", theorem on division by reciprocal
 //    refinement).  Zeros keep the sign of x (x/s with s > 0, so -0 stays
@@ -75,6 +75,8 @@ struct UnitScale {
   float y;     // RN(1/s)
   bool exact_div;
 
+  __device__ __forceinline__ UnitScale() : s(1.0f), y(1.0f), exact_div(false) {}
+  __device__ __forceinline__ UnitScale(float s_, float y_, bool e_) : s(s_), y(y_), exact_div(e_) {}
   __device__ __forceinline__ explicit UnitScale(float amax) {
     s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
     y = __frcp_rn(s);
@@ -95,23 +97,55 @@ struct UnitScale {
     return q;
   }
 
-  __device__ __forceinline__ float div_exact(float x) const { return __fdiv_rn(x, s); }
-
-  template <bool kExact>
-  __device__ __forceinline__ float div(float x) const {
-    if constexpr (kExact) return div_exact(x);
-    else return div_fast(x);
+  // The same two steps on a pair (x = {lo, hi}, nx = {-lo, -hi}); q - r'*y
+  // is written fma(r', -y, q), which is the same product and the same rounding.
+  __device__ __forceinline__ uint64_t div_fast2(uint64_t x, uint64_t nx) const {
+    const uint64_t ss = ptx::f2_pack(s, s), yy = ptx::f2_pack(y, y), nyy = ptx::f2_pack(-y, -y);
+    uint64_t q = ptx::f2_mul(x, yy);
+    uint64_t r = ptx::f2_fma(ss, q, nx);
+    q = ptx::f2_fma(r, nyy, q);
+    r = ptx::f2_fma(ss, q, nx);
+    q = ptx::f2_fma(r, nyy, q);
+    return q;
   }
+
+  __device__ __forceinline__ float div_exact(float x) const { return __fdiv_rn(x, s); }
 };
+
+// Two packed 16-bit inputs -> {x_lo, x_hi} and {-x_lo, -x_hi} as FP32 pairs.
+template <int DT>
+__device__ __forceinline__ void unpack2_pm(uint32_t w, uint64_t& x, uint64_t& nx) {
+  if constexpr (DT == kInF16) {
+    const float2 f = unpack2<DT>(w);
+    x = ptx::f2_pack(f.x, f.y);
+    nx = ptx::f2_pack(-f.x, -f.y);
+  } else {
+    const uint32_t lo = w << 16, hi = w & 0xFFFF0000u;
+    x = ptx::f2_pack(__uint_as_float(lo), __uint_as_float(hi));
+    nx = ptx::f2_pack(__uint_as_float(lo ^ 0x80000000u), __uint_as_float(hi ^ 0x80000000u));
+  }
+}
+
+// Two packed 16-bit inputs -> two E4M3 bytes (low input in the low byte).
+template <int DT, bool kExact>
+__device__ __forceinline__ uint32_t quant2(uint32_t w, const UnitScale& us) {
+  if constexpr (kExact) {
+    const float2 f = unpack2<DT>(w);
+    return ptx::cvt_e4m3x2(us.div_exact(f.y), us.div_exact(f.x));
+  } else {
+    uint64_t x, nx;
+    unpack2_pm<DT>(w, x, nx);
+    float lo, hi;
+    ptx::f2_unpack(us.div_fast2(x, nx), lo, hi);
+    return ptx::cvt_e4m3x2(hi, lo);
+  }
+}
 
 // 8 input elements (one 16-byte vector) -> 8 E4M3 bytes.
 template <int DT, bool kExact>
 __device__ __forceinline__ uint2 quant8_impl(const uint4& v, const UnitScale& us) {
-  const float2 a = unpack2<DT>(v.x), b = unpack2<DT>(v.y), c = unpack2<DT>(v.z), d = unpack2<DT>(v.w);
-  const uint32_t p0 = ptx::cvt_e4m3x2(us.div<kExact>(a.y), us.div<kExact>(a.x));
-  const uint32_t p1 = ptx::cvt_e4m3x2(us.div<kExact>(b.y), us.div<kExact>(b.x));
-  const uint32_t p2 = ptx::cvt_e4m3x2(us.div<kExact>(c.y), us.div<kExact>(c.x));
-  const uint32_t p3 = ptx::cvt_e4m3x2(us.div<kExact>(d.y), us.div<kExact>(d.x));
+  const uint32_t p0 = quant2<DT, kExact>(v.x, us), p1 = quant2<DT, kExact>(v.y, us);
+  const uint32_t p2 = quant2<DT, kExact>(v.z, us), p3 = quant2<DT, kExact>(v.w, us);
   return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
 }
 
@@ -139,39 +173,109 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 }
 
 // ------------------------------------------------------------------------
-// K3: one 1x128 token group per half-warp (16 lanes x 8 elements).
-// grid = (ceil(M/16/ROWS_PER_CTA_ITEMS) , K/128); the CTA (256 threads =
-// 16 half-warps) handles UNROLL blocks of 16 consecutive rows of one group
-// column, so each warp's 16 scale writes of a group column are contiguous.
-template <int DT, int UNROLL>
-__global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __restrict__ x,
-                                                                uint2* __restrict__ q,
-                                                                float* __restrict__ sa, int M, int G) {
-  const int hw = threadIdx.x >> 4;  // half-warp 0..15
-  const int hl = threadIdx.x & 15;  // lane within the half-warp
-  const int g = blockIdx.y;
-  const int64_t row_vec = static_cast<int64_t>(G) * 16;  // 16-byte vectors per row
-  int rows[UNROLL];
-  uint4 v[UNROLL];
-#pragma unroll
-  for (int u = 0; u < UNROLL; ++u) {
-    rows[u] = (blockIdx.x * UNROLL + u) * 16 + hw;
-    v[u] = make_uint4(0, 0, 0, 0);
-    if (rows[u] < M) v[u] = ld_stream(x + rows[u] * row_vec + g * 16 + hl);
+// K3: per-token 1x128 groups.  Rows of A are contiguous, so the M*K/128
+// groups form one contiguous sequence (group f = row f / G, column block
+// f % G, starting at element 128 f).  Persistent CTAs of 8 consumer warps +
+// 1 producer warp: the producer streams chunks of 128 consecutive groups
+// (32 KB of FP16/BF16, one 1-D bulk copy each) into a kTgStages-deep
+// shared-memory ring.  Consumer warp w owns groups 16w .. 16w+15 of a chunk:
+//   1. eight 16-byte loads per lane (load j: group 2j on lanes 0-15, group
+//      2j+1 on lanes 16-31) into registers, then the stage is released;
+//      each half-warp reduces its group's amax with 4 shuffles;
+//   2. lane i (0-15) turns the amax of group i into its scale and correctly
+//      rounded reciprocal (one divide per group, not per lane) and stores
+//      the scale;
+//   3. every lane fetches its group's scale by shuffle and casts its 8
+//      elements per load.
+constexpr int kTgChunkGroups = 128;
+constexpr int kTgStages = 3;
+constexpr int kTgChunkBytes = kTgChunkGroups * 256;
+constexpr int kTgSmemBytes = 1024 + kTgStages * kTgChunkBytes + 64;
+
+template <int DT>
+__global__ void __launch_bounds__(288, 2)
+    quant_token_group_kernel(const uint8_t* __restrict__ x, uint2* __restrict__ q, float* __restrict__ sa,
+                             uint32_t M, uint32_t G, uint32_t num_groups, unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kTgStages * kTgChunkBytes);
+  uint64_t* empty_bar = full_bar + kTgStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t num_chunks = (num_groups + kTgChunkGroups - 1) / kTgChunkGroups;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTgStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 8);
+    }
+    ptx::fence_mbar_init();
   }
+  __syncthreads();
+
+  if (warp == 8) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (uint32_t c = blockIdx.x; c < num_chunks; c += gridDim.x, ++it) {
+        const int s = it % kTgStages;
+        if (!ptx::mbar_wait_bounded(&empty_bar[s], ((it / kTgStages) & 1) ^ 1, timeout_ns)) {
+          record_quant_error();
+          break;
+        }
+        const uint32_t ng = min(num_groups - c * kTgChunkGroups, static_cast<uint32_t>(kTgChunkGroups));
+        ptx::mbar_arrive_expect_tx(&full_bar[s], ng * 256);
+        ptx::bulk_load(smem + s * kTgChunkBytes, x + static_cast<uint64_t>(c) * kTgChunkBytes, ng * 256,
+                       &full_bar[s]);
+      }
+      // every issued copy lands before the CTA may exit
+      const uint32_t first = it > kTgStages ? it - kTgStages : 0;
+      for (uint32_t j = first; j < it; ++j)
+        if (!ptx::mbar_wait_bounded(&full_bar[j % kTgStages], (j / kTgStages) & 1, timeout_ns)) record_quant_error();
+    }
+  } else {
+    const int half = lane >> 4, hl = lane & 15;
+    uint32_t it = 0;
+    for (uint32_t c = blockIdx.x; c < num_chunks; c += gridDim.x, ++it) {
+      const int s = it % kTgStages;
+      if (!ptx::mbar_wait_bounded(&full_bar[s], (it / kTgStages) & 1, timeout_ns)) {
+        record_quant_error();
+        break;
+      }
+      const uint32_t gw = c * kTgChunkGroups + warp * 16;  // first group of this warp
+      const uint4* tile = reinterpret_cast<const uint4*>(smem + s * kTgChunkBytes) + warp * 16 * 16;
+      uint4 v[8];
+      uint32_t mine = 0;  // lanes 0-15: amax bits of group gw + lane
 #pragma unroll
-  for (int u = 0; u < UNROLL; ++u) {
-    uint32_t a = amax_bits8(v[u]);
-    a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
-    a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-    a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-    a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-    const UnitScale us(mag_to_float<DT>(a));
-    if (rows[u] < M) {
-      q[rows[u] * row_vec + g * 16 + hl] = quant8<DT>(v[u], us);
-      if (hl == 0) sa[static_cast<int64_t>(g) * M + rows[u]] = us.s;
+      for (int j = 0; j < 8; ++j) {
+        v[j] = tile[(2 * j + half) * 16 + hl];  // groups past the end hold stale data; never stored
+        uint32_t a = amax_bits8(v[j]);
+        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
+        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, a, 16);
+        if (lane == 2 * j) mine = a;
+        if (lane == 2 * j + 1) mine = other;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);
+
+      UnitScale own(mag_to_float<DT>(mine));
+      const uint32_t my_group = gw + hl;
+      if (lane < 16 && my_group < num_groups) {
+        const uint32_t m = my_group / G;
+        sa[static_cast<uint64_t>(my_group - m * G) * M + m] = own.s;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int src = 2 * j + half;
+        const UnitScale us(__shfl_sync(0xFFFFFFFFu, own.s, src), __shfl_sync(0xFFFFFFFFu, own.y, src),
+                           __shfl_sync(0xFFFFFFFFu, own.exact_div ? 1 : 0, src) != 0);
+        const uint32_t g = gw + src;
+        if (g < num_groups) q[static_cast<uint64_t>(g) * 16 + hl] = quant8<DT>(v[j], us);
+      }
     }
   }
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------------

@@ -120,6 +120,21 @@ FP8S_API fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const u
                             void* c, fp8s_dtype ct, int64_t M, int64_t N, int64_t K,
                             fp8s_scale_mode mode, fp8s_stream_t stream);
 
+/*
+ * fp8s_gemm_override -- tuning aid: makes every later fp8_gemm_scaled call on
+ * any device use output tiles of 128 x bn and split each tile's K range over
+ * `splits` CTAs of a thread-block cluster, or (pair != 0, splits == 1, bn >=
+ * 64) tiles of 256 x bn shared by a pair of CTAs, instead of the library's
+ * own choice.  bn in {32, 64, 128, 256}; splits in {1, 2, 4, 8}.  With
+ * splits > 1 every cluster must own a single output tile; a later call whose
+ * K has fewer 128-wide blocks than `splits`, or with more 128 x bn output
+ * tiles than the device can hold clusters of `splits` CTAs at once, fails
+ * with FP8S_ERR_SHAPE.  bn = 0 restores the automatic choice.
+ * Results stay within the documented tolerance for every setting; only
+ * speed changes.  Not thread-safe against concurrent GEMM calls.
+ */
+FP8S_API fp8s_status fp8s_gemm_override(int bn, int splits, int pair);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 FP8S_API const char* fp8s_status_string(fp8s_status status);
 

@@ -96,3 +96,15 @@ def test_oracle_is_not_linked_into_the_library(lib):
     assert "oracle_" not in out
     src = open(os.path.join(ROOT, "fp8_scaled_gemm_02_b300", "__init__.py")).read()
     assert "oracle" not in src.replace("no fallback", "")
+
+
+def test_gemm_override_argument_checks(lib):
+    assert lib.fp8s_gemm_override(3, 1, 0) == 2
+    assert lib.fp8s_gemm_override(256, 16, 0) == 2
+    assert lib.fp8s_gemm_override(256, 8, 0) == 0
+    assert lib.fp8s_gemm_override(128, 3, 0) == 2
+    assert lib.fp8s_gemm_override(128, 4, 0) == 0
+    assert lib.fp8s_gemm_override(128, 2, 1) == 2     # a pair does not also split K
+    assert lib.fp8s_gemm_override(32, 1, 1) == 2      # a pair needs bn >= 64
+    assert lib.fp8s_gemm_override(256, 1, 1) == 0
+    assert lib.fp8s_gemm_override(0, 0, 0) == 0
