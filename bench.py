@@ -48,7 +48,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=30000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -176,7 +176,7 @@ class ClockSampler(threading.Thread):
                 time.sleep(0.01)
             return
         cmd = ["nvidia-smi", "--query-gpu=pci.bus_id,clocks.sm,clocks.max.sm,clocks_event_reasons.active",
-               "--format=csv,noheader,nounits", "-lms", "100"]
+               "--format=csv,noheader,nounits", "-lms", "50"]
         try:
             proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception as e:

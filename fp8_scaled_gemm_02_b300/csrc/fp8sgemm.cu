@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <unordered_map>
 
 #include "../../include/fp8sgemm.h"
@@ -150,6 +151,39 @@ fp8s_status tensor_map_e4m3(const uint8_t* ptr, int64_t rows, int64_t cols, int 
   return tensor_map_2d(ptr, rows, cols, 1, box_rows, kBK, true, dev, out);
 }
 
+// Launches `kern` with programmatic stream serialization (it may start while
+// the previous kernel of the stream finishes; every kernel of this library
+// waits for it before touching global memory) and, for cluster > 1, a 1-D
+// cluster dimension.
+template <typename... KArgs, typename... Args>
+fp8s_status launch_ex(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st, int cluster,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8S_ERR_CUDA;
+  }
+  return FP8S_OK;
+}
+
 template <typename KernelT>
 fp8s_status ensure_smem_attr(KernelT kern, int bytes, bool* done_per_device) {
   int dev = 0;
@@ -163,21 +197,31 @@ fp8s_status ensure_smem_attr(KernelT kern, int bytes, bool* done_per_device) {
 }
 
 // ------------------------------------------------------------ quantizers
+template <int DT, int GPW>
+fp8s_status launch_token_group_gpw(const void* x, int64_t M, int64_t G, uint8_t* q, float* sa, cudaStream_t st,
+                                   const DeviceInfo& info) {
+  static bool attr_done[kMaxDevices] = {};
+  auto kern = quant_token_group_kernel<DT, GPW>;
+  if (fp8s_status s = ensure_smem_attr(kern, kTgSmemBytes, attr_done)) return s;
+  const int64_t groups = M * G;
+  const int64_t chunks = (groups + 8 * GPW - 1) / (8 * GPW);
+  const int64_t cap = 2LL * info.sms;
+  const unsigned grid = static_cast<unsigned>(chunks < cap ? chunks : cap);
+  return launch_ex(kern, grid, 288, kTgSmemBytes, st, 1, static_cast<const uint8_t*>(x), reinterpret_cast<uint2*>(q), sa,
+                   static_cast<uint32_t>(M), static_cast<uint32_t>(G), static_cast<uint32_t>(groups), kWaitTimeoutNs);
+}
+
+// Groups per consumer warp: the largest that still gives every SM two chunks.
 template <int DT>
 fp8s_status launch_token_group(const void* x, int64_t M, int64_t K, uint8_t* q, float* sa, cudaStream_t st,
                                const DeviceInfo& info) {
-  static bool attr_done[kMaxDevices] = {};
-  auto kern = quant_token_group_kernel<DT>;
-  if (fp8s_status s = ensure_smem_attr(kern, kTgSmemBytes, attr_done)) return s;
   const int64_t G = K / 128;
   const int64_t groups = M * G;
-  const int64_t chunks = (groups + kTgChunkGroups - 1) / kTgChunkGroups;
-  const int64_t cap = 2LL * info.sms;
-  const unsigned grid = static_cast<unsigned>(chunks < cap ? chunks : cap);
-  kern<<<grid, 288, kTgSmemBytes, st>>>(static_cast<const uint8_t*>(x), reinterpret_cast<uint2*>(q), sa,
-                                         static_cast<uint32_t>(M), static_cast<uint32_t>(G),
-                                         static_cast<uint32_t>(groups), kWaitTimeoutNs);
-  return launch_status();
+  const int64_t want = 2LL * info.sms;
+  if (groups >= want * 8 * 16) return launch_token_group_gpw<DT, 16>(x, M, G, q, sa, st, info);
+  if (groups >= want * 8 * 8) return launch_token_group_gpw<DT, 8>(x, M, G, q, sa, st, info);
+  if (groups >= want * 8 * 4) return launch_token_group_gpw<DT, 4>(x, M, G, q, sa, st, info);
+  return launch_token_group_gpw<DT, 2>(x, M, G, q, sa, st, info);
 }
 
 template <int DT>
@@ -189,11 +233,10 @@ fp8s_status launch_weight_block(const void* w, int64_t N, int64_t K, uint8_t* q,
   auto kern = quant_weight_block_tma_kernel<DT>;
   if (fp8s_status s = ensure_smem_attr(kern, kWbSmemBytes, attr_done)) return s;
   const int64_t nblocks = ((N + 127) / 128) * (K / 128);
-  const int64_t cap = 2LL * info.sms;
+  const int64_t cap = info.sms;  // one CTA per SM
   const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
-  kern<<<grid, 288, kWbSmemBytes, st>>>(mw, reinterpret_cast<uint2*>(q), sb, static_cast<int>(N),
-                                         static_cast<int>(K / 128), static_cast<int>(nblocks), kWaitTimeoutNs);
-  return launch_status();
+  return launch_ex(kern, grid, kWbThreads, kWbSmemBytes, st, 1, mw, reinterpret_cast<uint2*>(q), sb, static_cast<int>(N),
+                   static_cast<int>(K / 128), static_cast<int>(nblocks), kWaitTimeoutNs);
 }
 
 template <int DT>
@@ -208,12 +251,14 @@ fp8s_status launch_per_tensor(const void* x, int64_t numel, uint8_t* q, float* s
   const int64_t cap = static_cast<int64_t>(info.sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  amax_kernel<DT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint4*>(x), nvec, tail, ntail,
-                                                                  word);
-  cast_per_tensor_kernel<DT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-      static_cast<const uint4*>(x), nvec, tail, ntail, reinterpret_cast<uint2*>(q), q + nvec * 8, word);
-  finalize_scale_kernel<<<1, 1, 0, st>>>(word);
-  return launch_status();
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (fp8s_status s = launch_ex(amax_kernel<DT>, g, 256, 0, st, 1, static_cast<const uint4*>(x), nvec, tail, ntail, word))
+    return s;
+  if (fp8s_status s = launch_ex(cast_per_tensor_kernel<DT>, g, 256, 0, st, 1, static_cast<const uint4*>(x), nvec, tail,
+                                ntail, reinterpret_cast<uint2*>(q), q + nvec * 8,
+                                static_cast<const unsigned int*>(word)))
+    return s;
+  return launch_ex(finalize_scale_kernel, 1, 1, 0, st, 1, word);
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -273,44 +318,19 @@ fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const 
     const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, 2, dev, info.sms);
     if (cmax < 1) return FP8S_ERR_CUDA;
     const int clusters = p.num_tiles < cmax ? p.num_tiles : cmax;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(Cfg::kThreads), 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(Cfg::kSmemBytes);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, ma, mb, p) != cudaSuccess) return launch_status(), FP8S_ERR_CUDA;
+    return launch_ex(kern, static_cast<unsigned>(clusters * 2), Cfg::kThreads, Cfg::kSmemBytes, st, 2, ma, mb, p);
   } else if constexpr (!SPLIT) {
     const int grid = p.num_tiles < info.sms ? p.num_tiles : info.sms;
-    kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
+    return launch_ex(kern, static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, st, 1, ma, mb, p);
   } else {
     const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, splits, dev, info.sms);
     if (cmax < 1) return FP8S_ERR_CUDA;
     // one tile per cluster: the kernel stages its split-K partials in the
     // operand ring, which only drains for good after a cluster's last tile
     if (p.num_tiles > cmax) return FP8S_ERR_SHAPE;
-    const int clusters = p.num_tiles;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * splits), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(Cfg::kThreads), 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(Cfg::kSmemBytes);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, ma, mb, p) != cudaSuccess) return launch_status(), FP8S_ERR_CUDA;
+    return launch_ex(kern, static_cast<unsigned>(p.num_tiles * splits), Cfg::kThreads, Cfg::kSmemBytes, st, splits, ma,
+                     mb, p);
   }
-  return launch_status();
 }
 
 // Relative tensor-pipe efficiency of one 128 x BN x 128 K block, measured on
@@ -329,7 +349,7 @@ GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms) {
   const int64_t tm = (M + kBM - 1) / kBM;
   for (int bn : bns) {
     for (int s = 1; s <= 8; s *= 2) {
-      if (s > KB) continue;
+      if (s > KB || (s > 1 && bn > 192)) continue;
       const int64_t tiles = tm * ((N + bn - 1) / bn);
       const int64_t clusters = sms / s;
       if (s > 1 && tiles > clusters * 7 / 8) continue;  // split-K needs one tile per cluster (with slack for GPC packing)
@@ -354,6 +374,7 @@ fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUt
     switch (ch.bn) {
       case 64: return launch_gemm_cfg<64, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
       case 128: return launch_gemm_cfg<128, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+      case 192: return launch_gemm_cfg<192, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
       case 256: return launch_gemm_cfg<256, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
       default: return FP8S_ERR_SHAPE;
     }
@@ -363,7 +384,7 @@ fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUt
       case 32: return launch_gemm_cfg<32, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
       case 64: return launch_gemm_cfg<64, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
       case 128: return launch_gemm_cfg<128, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
-      case 256: return launch_gemm_cfg<256, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
+      case 192: return launch_gemm_cfg<192, MODE, OUT, true, false>(ma, mb, p, ch.splits, info, dev, st);
       default: return FP8S_ERR_SHAPE;
     }
   }
@@ -371,6 +392,7 @@ fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUt
     case 32: return launch_gemm_cfg<32, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
     case 64: return launch_gemm_cfg<64, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
     case 128: return launch_gemm_cfg<128, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
+    case 192: return launch_gemm_cfg<192, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
     case 256: return launch_gemm_cfg<256, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
     default: return FP8S_ERR_SHAPE;
   }
@@ -497,9 +519,11 @@ fp8s_status fp8s_gemm_override(int bn, int splits, int pair) {
     g_force_pair = 0;
     return FP8S_OK;
   }
-  if ((bn != 32 && bn != 64 && bn != 128 && bn != 256) || (splits != 1 && splits != 2 && splits != 4 && splits != 8))
+  if ((bn != 32 && bn != 64 && bn != 128 && bn != 192 && bn != 256) ||
+      (splits != 1 && splits != 2 && splits != 4 && splits != 8))
     return FP8S_ERR_SHAPE;
   if (pair && (splits != 1 || bn < 64)) return FP8S_ERR_SHAPE;
+  if (splits > 1 && bn > 192) return FP8S_ERR_SHAPE;  // split-K exchanges the partial tile in one pass
   g_force_bn = bn;
   g_force_splits = splits;
   g_force_pair = pair ? 1 : 0;

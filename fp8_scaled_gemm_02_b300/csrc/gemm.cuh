@@ -86,50 +86,62 @@ struct GemmParams {
 
 template <int BN, int MODE, bool SPLIT, bool PAIR = false>
 struct GemmCfg {
-  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN");
+  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 192 || BN == 256, "BN");
   static_assert(!(SPLIT && PAIR), "a CTA pair does not also split K");
   static_assert(!PAIR || BN >= 64, "a CTA pair holds at least 32 rows of B each");
-  // Block mode keeps 64 FP32 accumulators per epilogue thread: BN = 256
-  // needs four epilogue warpgroups.
-  static constexpr int kEpiWarps = (MODE == kModeBlock && BN == 256) ? 16 : 8;
+  // Block mode keeps the tile's FP32 accumulators in the epilogue threads'
+  // registers: BN = 256 uses four epilogue warpgroups (64 columns each);
+  // BN = 192 uses six (32 columns each, so one TMEM load covers a thread's
+  // share of a K block).
+  static constexpr int kEpiWarps = MODE != kModeBlock ? 8 : BN == 256 ? 16 : BN == 192 ? 24 : 8;
   static constexpr int kEpiWG = kEpiWarps / 4;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kThreads = 128 + kEpiThreads;
   static constexpr bool kLowReg = kEpiWarps == 16;  // 640 threads: at most 96 registers each
+  // Block mode with 16 or 24 epilogue warps (at most 96 or 72 registers a
+  // thread) reads a K block's partial 16 columns per wait, so only one chunk
+  // is staged next to the accumulators.
+  static constexpr bool kSeqChunks = MODE == kModeBlock && kEpiWarps >= 12;
+  // Columns of a K block's partial loaded per wait.
+  static constexpr int kSeqLoadCols = 16;
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;   // output rows per (pair) tile
   static constexpr int kBRows = PAIR ? BN / 2 : BN;     // rows of B this CTA loads
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = kBRows * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  // Split-K partial: exchanged in passes of up to 128 columns (128 rows x
-  // 128 FP32 = 64 KB of shared memory), rows padded by 4 words so that
-  // 16-byte writes of 8 consecutive rows cover all 32 banks.
-  static constexpr int kPassCols = BN < 128 ? BN : 128;
-  static constexpr int kPasses = BN / kPassCols;
-  static constexpr int kStagePitch = kPassCols + 4;
-  static constexpr int kStagingBytes = kBM * kStagePitch * 4;  // aliases the operand ring
-  static constexpr int kStagesRaw = (210 * 1024) / kStageBytes;
+  // Split-K partial: 128 rows x BN FP32, rows padded by 4 words so that
+  // 16-byte writes of 8 consecutive rows cover all 32 banks.  The outgoing
+  // partial aliases the drained operand ring; the incoming slices of up to 7
+  // peers (at most 112 rows in all) have a buffer of their own.
+  static_assert(!SPLIT || BN <= 192, "split-K exchanges a 128 x BN partial in one pass");
+  static constexpr int kStagePitch = BN + 4;
+  static constexpr int kStagingBytes = kBM * kStagePitch * 4;
+  static constexpr int kRecvBytes = SPLIT ? 112 * kStagePitch * 4 : 0;
+  static constexpr int kStagesRaw = (214 * 1024 - kRecvBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(!SPLIT || kStages * kStageBytes >= kStagingBytes, "staging fits in the ring");
   // TMEM accumulator buffers: whole tiles (per-tensor) or single K blocks
   // (block mode; narrow tiles get up to 16 so the MMA can run far ahead).
   static constexpr int kNBufMax = MODE == kModeBlock ? 16 : 4;
-  static constexpr int kTmemMax = PAIR ? 256 : 512;
+  static constexpr int kTmemMax = 512;
   static constexpr int kNBuf = (kTmemMax / BN) > kNBufMax ? kNBufMax : (kTmemMax / BN);
   static constexpr int kTmemCols = kNBuf * BN;
+  static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
+                                  : kTmemCols <= 256 ? 256 : 512;  // allocations are powers of two
   static constexpr int kColsPerThread = BN / kEpiWG;
-  static constexpr int kChunk = kLowReg ? 16 : (kColsPerThread < 32 ? kColsPerThread : 32);
+  static constexpr int kChunk = (kLowReg || kEpiWarps == 24) ? 16 : (kColsPerThread < 32 ? kColsPerThread : 32);
+  static_assert(kColsPerThread % kChunk == 0, "chunks tile a thread's columns");
   // Block mode: K blocks the epilogue takes per TMEM hand-off (one
   // tcgen05.wait::ld per batch), capped by registers and by half the buffers.
   static constexpr int kBatchRaw = 64 / kColsPerThread;
   static constexpr int kBatch =
-      (MODE == kModeBlock && !kLowReg) ? (kBatchRaw > kNBuf / 2 ? kNBuf / 2 : kBatchRaw) : 1;
+      (MODE == kModeBlock && !kSeqChunks) ? (kBatchRaw > kNBuf / 2 ? kNBuf / 2 : kBatchRaw) : 1;
   static_assert(kBatch >= 1, "batch");
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 1 + 2) + 16;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRecvBytes + kBarBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
+  static_assert(kTmemCols <= 512, "TMEM columns");
 };
 
 // First K block (within the CTA's K range) of a tile.  Tiles start their K
@@ -224,32 +236,82 @@ __device__ __forceinline__ void stage_row(float* srow, const float* v) {
   for (int j = 0; j < W; j += 4) *reinterpret_cast<float4*>(srow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
 }
 
-// Split-K reduction: this CTA's rows of one column pass (columns col0 ..
-// col0 + PASS_COLS of the tile), summed over the S partials of the cluster
-// in rank order, rounded and stored.  `tid` indexes the epilogue threads.
-template <int BN, int PASS_COLS, int OUT>
-__device__ __forceinline__ void reduce_partials(uint32_t staging_addr, uint32_t rank, uint32_t S, int tid,
-                                                int nthreads, int tm, int tn, int col0, const GemmParams& p) {
-  constexpr int kPitch = PASS_COLS + 4;
-  constexpr int kVecPerRow = PASS_COLS / 4;
-  const int rows = kBM / static_cast<int>(S);
-  const int row0 = static_cast<int>(rank) * rows;
+// Tells the MMA issuer a TMEM accumulator buffer has been read.  In a CTA
+// pair the issuer (and the barrier) lives in the leader CTA.
+template <bool PAIR>
+__device__ __forceinline__ void release_tmem(uint64_t* bar) {
+  // The TMEM reads are ordered by tcgen05.wait::ld and the before-sync fence
+  // the caller issued; no memory operation needs releasing.
+  if constexpr (PAIR) ptx::mbar_arrive_cluster_relaxed(ptx::mapa(ptx::smem_u32(bar), 0));
+  else ptx::mbar_arrive(bar);
+}
+
+// Split-K exchange, pushed through the cluster's shared memory.  Rank r of
+// S owns output rows [r*R, (r+1)*R), R = 128/S.  Once every epilogue warp of
+// this CTA has written its part of the partial into `send` (signalled on the
+// CTA-local `staged` barrier), one thread copies the R-row slice owned by
+// each peer q straight into q's receive buffer with a bulk copy
+// (cp.async.bulk shared::cta -> shared::cluster) that completes on q's
+// `recv` barrier; the data arriving is the signal.  Each CTA then waits for
+// its S-1 incoming slices, sums its rows over all S partials in rank order
+// (local shared memory only), rounds and stores.  Slot j of the receive
+// buffer holds the slice of peer q, j = q < r ? q : q - 1.  Every wait is
+// bounded; returns false (after recording the error) if one gave up.
+template <int BN, int OUT>
+__device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64_t* recv_bar, const float* send,
+                                                    const float* recv, uint32_t rank, uint32_t S, int tid,
+                                                    int nthreads, int tm, int tn, const GemmParams& p) {
+  constexpr int kPitch = BN + 4;
+  constexpr int kVecPerRow = BN / 4;
+  const int R = kBM / static_cast<int>(S);
+  const uint32_t slice_bytes = static_cast<uint32_t>(R * kPitch * 4);
+  const int lane = tid & 31;
+  ptx::fence_proxy_async_shared();  // this thread's ordinary stores, before the bulk copies read them
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(staged_bar);
+  if (tid == 0) {
+    if (!ptx::mbar_wait_bounded(staged_bar, 0, p.timeout_ns)) {
+      record_error(kErrEpilogue);
+      return false;
+    }
+    // After the staged wait, so that threads which see `recv` complete also
+    // see every warp's part of this CTA's own slice.  Incoming bytes may land
+    // before this; the phase cannot complete until this arrival.
+    ptx::mbar_arrive_expect_tx(recv_bar, (S - 1) * slice_bytes);
+    const uint32_t send0 = ptx::smem_u32(send), recv0 = ptx::smem_u32(recv), rbar = ptx::smem_u32(recv_bar);
+    for (uint32_t q = 0; q < S; ++q) {
+      if (q == rank) continue;
+      const uint32_t slot = rank < q ? rank : rank - 1;  // this CTA's slot in q's receive buffer
+      ptx::bulk_copy_to_peer(ptx::mapa(recv0 + slot * slice_bytes, q), send0 + q * slice_bytes, slice_bytes,
+                             ptx::mapa(rbar, q));
+    }
+  }
+  if (!ptx::mbar_wait_bounded(recv_bar, 0, p.timeout_ns)) {
+    record_error(kErrEpilogue);
+    return false;
+  }
   uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
   const bool vec_ok = (p.N % 4) == 0;
-  for (int v = tid; v < rows * kVecPerRow; v += nthreads) {
-    const int r = row0 + v / kVecPerRow;
+  const int total = R * kVecPerRow;
+  for (int v = tid; v < total; v += nthreads) {
+    const int rl = v / kVecPerRow;           // row within the slice
     const int c4 = (v % kVecPerRow) * 4;
-    const uint32_t off = staging_addr + static_cast<uint32_t>((r * kPitch + c4) * 4);
-    float4 acc = ptx::ld_dsmem_f4(ptx::mapa(off, 0));
-    for (uint32_t q = 1; q < S; ++q) {
-      const float4 t = ptx::ld_dsmem_f4(ptx::mapa(off, q));
-      acc.x += t.x;
-      acc.y += t.y;
-      acc.z += t.z;
-      acc.w += t.w;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (uint32_t q = 0; q < S; ++q) {
+      const float* src = q == rank ? send + (static_cast<int>(rank) * R + rl) * kPitch
+                                   : recv + ((q < rank ? q : q - 1) * R + rl) * kPitch;
+      const float4 t = *reinterpret_cast<const float4*>(src + c4);
+      if (q == 0) {
+        acc = t;
+      } else {
+        acc.x += t.x;
+        acc.y += t.y;
+        acc.z += t.z;
+        acc.w += t.w;
+      }
     }
-    const int row = tm * kBM + r;
-    const int n = tn * BN + col0 + c4;
+    const int row = tm * kBM + static_cast<int>(rank) * R + rl;
+    const int n = tn * BN + c4;
     if (row >= p.M) continue;
     uint16_t* crow = C + static_cast<int64_t>(row) * p.N;
     if (vec_ok && n + 4 <= p.N) {
@@ -264,32 +326,6 @@ __device__ __forceinline__ void reduce_partials(uint32_t staging_addr, uint32_t 
         if (n + j < p.N) crow[n + j] = one_out<OUT>(a4[j]);
     }
   }
-}
-
-// Tells the MMA issuer a TMEM accumulator buffer has been read.  In a CTA
-// pair the issuer (and the barrier) lives in the leader CTA.
-template <bool PAIR>
-__device__ __forceinline__ void release_tmem(uint64_t* bar) {
-  if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(bar), 0));
-  else ptx::mbar_arrive(bar);
-}
-
-// Split-K hand-off of one column pass: publish this CTA's staged partial to
-// every CTA of the cluster, wait until all S partials are staged, reduce this
-// CTA's rows, then tell every CTA that its partial has been read.  Returns
-// false (after recording the error) if the wait gave up.
-template <int BN, int OUT>
-__device__ __forceinline__ bool exchange_and_reduce(uint64_t* ready_bar, uint64_t* done_bar, uint32_t staging_addr,
-                                                    uint32_t rank, uint32_t S, int tid, int nthreads, int tm, int tn,
-                                                    int pass, uint32_t it, const GemmParams& p) {
-  constexpr int kPassCols = BN < 128 ? BN : 128;
-  for (uint32_t q = 0; q < S; ++q) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(ready_bar), q));
-  if (!ptx::mbar_wait_cluster_bounded(ready_bar, it & 1, p.timeout_ns)) {
-    record_error(kErrEpilogue);
-    return false;
-  }
-  reduce_partials<BN, kPassCols, OUT>(staging_addr, rank, S, tid, nthreads, tm, tn, pass * kPassCols, p);
-  for (uint32_t q = 0; q < S; ++q) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(done_bar), q));
   return true;
 }
 
@@ -309,14 +345,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + S_ * Cfg::kABytes;
   float* staging = reinterpret_cast<float*>(smem);  // split-K only: used after the ring has drained
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + S_ * Cfg::kBBytes);
+  const float* recv = reinterpret_cast<const float*>(smem + S_ * Cfg::kStageBytes);  // split-K incoming slices
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + S_ * Cfg::kBBytes + Cfg::kRecvBytes);
   uint64_t* empty_bar = full_bar + S_;
   uint64_t* tfull_bar = empty_bar + S_;
   uint64_t* tempty_bar = tfull_bar + NBUF;
   uint64_t* mma_done_bar = tempty_bar + NBUF;
-  uint64_t* ready_bar = mma_done_bar + 1;  // split-K: all S partials of the tile are staged
-  uint64_t* done_bar = ready_bar + 1;      // split-K: all S CTAs finished reading this CTA's partial
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* staged_bar = mma_done_bar + 1;  // split-K: every epilogue warp of this CTA staged its part
+  uint64_t* recv_bar = staged_bar + 1;      // split-K: all S-1 incoming slices have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
   volatile uint32_t* pair_bad = tmem_slot + 1;  // CTA pair: the two TMEM allocations disagree
 
   const int warp = threadIdx.x >> 5;
@@ -356,22 +393,27 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
       ptx::mbar_init(&tempty_bar[b], (PAIR ? 2 : 1) * Cfg::kEpiWarps);
     }
     ptx::mbar_init(mma_done_bar, 1);
-    ptx::mbar_init(ready_bar, S * Cfg::kEpiThreads);
-    ptx::mbar_init(done_bar, S * Cfg::kEpiThreads);
+    ptx::mbar_init(staged_bar, Cfg::kEpiWarps);
+    ptx::mbar_init(recv_bar, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
     if constexpr (PAIR) {
-      ptx::tmem_alloc_pair<Cfg::kTmemCols>(tmem_slot);
+      ptx::tmem_alloc_pair<Cfg::kTmemAlloc>(tmem_slot);
       ptx::tmem_relinquish_pair();
     } else {
-      ptx::tmem_alloc<Cfg::kTmemCols>(tmem_slot);
+      ptx::tmem_alloc<Cfg::kTmemAlloc>(tmem_slot);
       ptx::tmem_relinquish();
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if constexpr (SPLIT || PAIR) ptx::cluster_sync_all();  // peers' barriers are initialised before any remote arrive
+  // Peers' barriers must be initialised before any remote arrive.  A pair
+  // signals its peer from the first K block on; split-K only in the
+  // epilogue, so there the wait is deferred until the first exchange.
+  if constexpr (PAIR) ptx::cluster_sync_all();
+  if constexpr (SPLIT) ptx::cluster_arrive_relaxed();
+  bool cluster_waited = !SPLIT;
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if constexpr (PAIR) {
@@ -385,6 +427,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
     __syncthreads();
   }
   const bool run_roles = !(PAIR && *pair_bad);
+  ptx::griddep_wait();  // the previous kernel's writes (our operands) are visible from here on
+  ptx::griddep_launch();
 
   if (!run_roles) {
     // nothing: the CTA pair could not share its accumulators
@@ -496,13 +540,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const bool vec_ok = (p.N % 8) == 0;
     uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
-    // split-K: this thread's columns go to staging pass wg*CPT / kPassCols
-    constexpr int kPassCols = Cfg::kPassCols;
-    const int my_pass = (wg * CPT) / kPassCols;
-    float* srow = staging + row_local * Cfg::kStagePitch + (wg * CPT - my_pass * kPassCols);
-    const uint32_t staging_addr = ptx::smem_u32(staging);
+    float* srow = staging + row_local * Cfg::kStagePitch + wg * CPT;  // split-K: this thread's partial row
     uint32_t unit = 0;
-    uint32_t it = 0;  // tiles this CTA has finished (split-K barrier phases)
     bool ok = true;
 
     float pt_scale = 0.0f;
@@ -524,29 +563,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
         }
         ptx::tc_fence_after();
         if constexpr (SPLIT) {
-          for (int h = 0; h < Cfg::kPasses && ok; ++h) {
-            if (it > 0 && !ptx::mbar_wait_cluster_bounded(done_bar, (it - 1) & 1, p.timeout_ns)) {
-              record_error(kErrEpilogue);
-              ok = false;
-              break;
-            }
-            if (my_pass == h) {
 #pragma unroll
-              for (int c = 0; c < CPT / CW; ++c) {
-                float v[CW];
-                tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
+          for (int c = 0; c < CPT / CW; ++c) {
+            float v[CW];
+            tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
 #pragma unroll
-                for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
-                stage_row<CW>(srow + c * CW, v);
-              }
-            }
-            if (!exchange_and_reduce<BN, OUT>(ready_bar, done_bar, staging_addr, rank, S, epi_tid,
-                                              Cfg::kEpiThreads, tm, tn, h, it, p)) {
-              ok = false;
-              break;
-            }
-            ++it;
+            for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
+            stage_row<CW>(srow + c * CW, v);
           }
+          if (!cluster_waited) {  // peers' barriers are initialised from here on
+            ptx::cluster_wait();
+            cluster_waited = true;
+          }
+          if (!exchange_and_reduce<BN, OUT>(staged_bar, recv_bar, staging, recv, rank, S, epi_tid, Cfg::kEpiThreads,
+                                            tm, tn, p))
+            ok = false;
         } else {
 #pragma unroll
           for (int c = 0; c < CPT / CW; ++c) {
@@ -567,7 +598,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
         float acc[CPT];
 #pragma unroll
         for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
-        const int nb = n_base / 128;  // weight block row of this warpgroup's columns
+        // weight block row of this warpgroup's columns (clamped: a slice past
+        // the last column of a ragged tile is computed but never stored)
+        const int nb = (n_base < p.N ? n_base : p.N - 1) / 128;
         const float* sa_col = p.sa + (row < p.M ? row : 0);
         const float* sb_row = p.sb + static_cast<int64_t>(nb) * p.num_kb;
         const int rot = kb_rotation(tm, tn, nkb);
@@ -598,22 +631,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
           }
           if (!ok) break;
           ptx::tc_fence_after();
-          if constexpr (Cfg::kLowReg) {
-            // One K block at a time, 16 columns per TMEM load: 64
-            // accumulators + 16 staged values fit the 96-register budget.
+          if constexpr (Cfg::kSeqChunks) {
+            // One K block at a time, kSeqLoadCols columns per wait: the
+            // accumulators + the staged columns fit the register budget.
+            constexpr int LC = Cfg::kSeqLoadCols;
             const uint32_t col0 = (unit % NBUF) * BN + wg * CPT;
 #pragma unroll
-            for (int c = 0; c < CPT / CW; ++c) {
-              uint32_t part[CW];
-              tmem_load_nowait<CW>(tmem_base + lane_off + col0 + c * CW, part);
+            for (int c0 = 0; c0 < CPT; c0 += LC) {
+              uint32_t part[LC];
+#pragma unroll
+              for (int c = 0; c < LC; c += CW) tmem_load_nowait<CW>(tmem_base + lane_off + col0 + c0 + c, &part[c]);
               ptx::tmem_ld_wait();
-              if (c == CPT / CW - 1) {
+              if (c0 + LC == CPT) {
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_tmem<PAIR>(&tempty_bar[unit % NBUF]);
               }
 #pragma unroll
-              for (int j = 0; j < CW; j += 2) promote2(&acc[c * CW + j], part[j], part[j + 1], sc[0]);
+              for (int j = 0; j < LC; j += 2) promote2(&acc[c0 + j], part[j], part[j + 1], sc[0]);
             }
             unit += 1;
           } else {
@@ -643,20 +678,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
         }
         if (!ok) break;
         if constexpr (SPLIT) {
-          for (int h = 0; h < Cfg::kPasses && ok; ++h) {
-            if (it > 0 && !ptx::mbar_wait_cluster_bounded(done_bar, (it - 1) & 1, p.timeout_ns)) {
-              record_error(kErrEpilogue);
-              ok = false;
-              break;
-            }
-            if (my_pass == h) stage_row<CPT>(srow, acc);
-            if (!exchange_and_reduce<BN, OUT>(ready_bar, done_bar, staging_addr, rank, S, epi_tid,
-                                              Cfg::kEpiThreads, tm, tn, h, it, p)) {
-              ok = false;
-              break;
-            }
-            ++it;
+          stage_row<CPT>(srow, acc);
+          if (!cluster_waited) {  // peers' barriers are initialised from here on
+            ptx::cluster_wait();
+            cluster_waited = true;
           }
+          if (!exchange_and_reduce<BN, OUT>(staged_bar, recv_bar, staging, recv, rank, S, epi_tid, Cfg::kEpiThreads,
+                                            tm, tn, p))
+            ok = false;
           if (!ok) break;
         } else {
           if (row < p.M) {
@@ -667,21 +696,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
       }
 
     }
-    if constexpr (SPLIT) {
-      // Nobody may still be reading this CTA's partial when it exits.
-      if (ok && it > 0 && !ptx::mbar_wait_cluster_bounded(done_bar, (it - 1) & 1, p.timeout_ns))
-        record_error(kErrEpilogue);
-    }
   }
 
+  if (!cluster_waited) ptx::cluster_wait();  // every thread waits out its split-K arrival before the last barrier
   ptx::tc_fence_before();
   __syncthreads();
   // A pair frees its TMEM together, after both CTAs are done with it.
   if constexpr (PAIR) ptx::cluster_sync_all();
   if (warp == 2) {
     ptx::tc_fence_after();
-    if constexpr (PAIR) ptx::tmem_dealloc_pair<Cfg::kTmemCols>(tmem_base);
-    else ptx::tmem_dealloc<Cfg::kTmemCols>(tmem_base);
+    if constexpr (PAIR) ptx::tmem_dealloc_pair<Cfg::kTmemAlloc>(tmem_base);
+    else ptx::tmem_dealloc<Cfg::kTmemAlloc>(tmem_base);
   }
   if constexpr (SPLIT || PAIR) ptx::cluster_sync_all();  // no CTA leaves while a peer may touch its shared memory
 }

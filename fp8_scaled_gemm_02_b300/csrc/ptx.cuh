@@ -76,6 +76,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in the stream is still running.  griddep_wait blocks
+// until that kernel has completed and its memory is visible (a no-op when
+// there is none); griddep_launch lets the next kernel start launching once
+// every CTA of this grid has issued it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -101,17 +110,37 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split form of the cluster barrier: arrive (relaxed; a preceding
+// fence.mbarrier_init or other release fence orders what must be visible)
+// now, wait later, so the wait overlaps other work.  Every thread that
+// arrives must wait before it arrives again.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Named barrier over `nthreads` threads (a multiple of 32) of this CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Arrive on an mbarrier that may live in another CTA of the cluster; this
 // thread's earlier memory operations are released at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+// Arrive without ordering any memory operation (for hand-offs whose
+// ordering comes from elsewhere, e.g. tcgen05 fences for TMEM).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_relaxed_cluster(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar_addr), "r"(parity)
@@ -119,17 +148,23 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_
   return ok != 0;
 }
 
-// As mbar_wait_bounded, acquiring at cluster scope (the arrivals come from
-// other CTAs of the cluster).
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// As mbar_wait_bounded for arrivals from other CTAs of the cluster: polls
+// without ordering, then one cluster-scope fence makes what the arriving
+// CTAs released before their arrive visible (an acquire).
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait_cluster(a, parity)) return true;
-    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  bool done = mbar_try_wait_relaxed_cluster(a, parity);
+  if (!done) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!done) {
+      for (int i = 0; i < 256 && !done; ++i) done = mbar_try_wait_relaxed_cluster(a, parity);
+      if (!done && globaltimer_ns() - t0 > timeout_ns) return false;
+    }
   }
+  fence_acq_rel_cluster();
+  return true;
 }
 
 // 16-byte load from the shared memory of any CTA of the cluster.
@@ -165,6 +200,18 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(smem_dst)),
                "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into another CTA of the cluster
+// (both addresses 16-byte aligned, size a multiple of 16); completion is
+// signalled as transaction bytes on the destination CTA's mbarrier.  The
+// source must have been made visible to the async proxy (fence.proxy.async).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster_addr, uint32_t src_smem_addr, uint32_t bytes,
+                                                  uint32_t bar_cluster_addr) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster_addr),
+               "r"(src_smem_addr), "r"(bytes), "r"(bar_cluster_addr)
                : "memory");
 }
 

@@ -176,29 +176,33 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 // K3: per-token 1x128 groups.  Rows of A are contiguous, so the M*K/128
 // groups form one contiguous sequence (group f = row f / G, column block
 // f % G, starting at element 128 f).  Persistent CTAs of 8 consumer warps +
-// 1 producer warp: the producer streams chunks of 128 consecutive groups
-// (32 KB of FP16/BF16, one 1-D bulk copy each) into a kTgStages-deep
-// shared-memory ring.  Consumer warp w owns groups 16w .. 16w+15 of a chunk:
-//   1. eight 16-byte loads per lane (load j: group 2j on lanes 0-15, group
+// 1 producer warp: the producer streams chunks of 8*GPW consecutive groups
+// (GPW = 16: 32 KB of FP16/BF16, one 1-D bulk copy each) into a
+// kTgStages-deep shared-memory ring.  Consumer warp w owns groups
+// GPW*w .. GPW*w + GPW-1 of a chunk:
+//   1. GPW/2 16-byte loads per lane (load j: group 2j on lanes 0-15, group
 //      2j+1 on lanes 16-31) into registers, then the stage is released;
 //      each half-warp reduces its group's amax with 4 shuffles;
-//   2. lane i (0-15) turns the amax of group i into its scale and correctly
+//   2. lane i < GPW turns the amax of group i into its scale and correctly
 //      rounded reciprocal (one divide per group, not per lane) and stores
 //      the scale;
 //   3. every lane fetches its group's scale by shuffle and casts its 8
 //      elements per load.
-constexpr int kTgChunkGroups = 128;
+// Small tensors use a small GPW so that the chunks still cover every SM.
 constexpr int kTgStages = 3;
-constexpr int kTgChunkBytes = kTgChunkGroups * 256;
-constexpr int kTgSmemBytes = 1024 + kTgStages * kTgChunkBytes + 64;
+constexpr int kTgMaxChunkBytes = 8 * 16 * 256;
+constexpr int kTgSmemBytes = 1024 + kTgStages * kTgMaxChunkBytes + 64;
 
-template <int DT>
+template <int DT, int GPW>
 __global__ void __launch_bounds__(288, 2)
     quant_token_group_kernel(const uint8_t* __restrict__ x, uint2* __restrict__ q, float* __restrict__ sa,
                              uint32_t M, uint32_t G, uint32_t num_groups, unsigned long long timeout_ns) {
+  static_assert(GPW == 2 || GPW == 4 || GPW == 8 || GPW == 16, "groups per warp");
+  constexpr int kTgChunkGroups = 8 * GPW;
+  constexpr int kTgChunkBytes = kTgChunkGroups * 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kTgStages * kTgChunkBytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kTgStages * kTgMaxChunkBytes);
   uint64_t* empty_bar = full_bar + kTgStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,6 +215,8 @@ __global__ void __launch_bounds__(288, 2)
     ptx::fence_mbar_init();
   }
   __syncthreads();
+  ptx::griddep_wait();  // the previous kernel's writes are visible from here on
+  ptx::griddep_launch();
 
   if (warp == 8) {
     if (lane == 0) {
@@ -240,12 +246,12 @@ __global__ void __launch_bounds__(288, 2)
         record_quant_error();
         break;
       }
-      const uint32_t gw = c * kTgChunkGroups + warp * 16;  // first group of this warp
-      const uint4* tile = reinterpret_cast<const uint4*>(smem + s * kTgChunkBytes) + warp * 16 * 16;
-      uint4 v[8];
-      uint32_t mine = 0;  // lanes 0-15: amax bits of group gw + lane
+      const uint32_t gw = c * kTgChunkGroups + warp * GPW;  // first group of this warp
+      const uint4* tile = reinterpret_cast<const uint4*>(smem + s * kTgChunkBytes) + warp * GPW * 16;
+      uint4 v[GPW / 2];
+      uint32_t mine = 0;  // lanes 0..GPW-1: amax bits of group gw + lane
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < GPW / 2; ++j) {
         v[j] = tile[(2 * j + half) * 16 + hl];  // groups past the end hold stale data; never stored
         uint32_t a = amax_bits8(v[j]);
         a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
@@ -261,12 +267,12 @@ __global__ void __launch_bounds__(288, 2)
 
       UnitScale own(mag_to_float<DT>(mine));
       const uint32_t my_group = gw + hl;
-      if (lane < 16 && my_group < num_groups) {
+      if (lane < GPW && my_group < num_groups) {
         const uint32_t m = my_group / G;
         sa[static_cast<uint64_t>(my_group - m * G) * M + m] = own.s;
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < GPW / 2; ++j) {
         const int src = 2 * j + half;
         const UnitScale us(__shfl_sync(0xFFFFFFFFu, own.s, src), __shfl_sync(0xFFFFFFFFu, own.y, src),
                            __shfl_sync(0xFFFFFFFFu, own.exact_div ? 1 : 0, src) != 0);
@@ -279,20 +285,26 @@ __global__ void __launch_bounds__(288, 2)
 }
 
 // ------------------------------------------------------------------------
-// K4: persistent CTAs of 8 consumer warps + 1 TMA producer warp.  The
-// producer streams whole 128x128 weight blocks (32 KB of FP16/BF16, one 2-D
-// TMA box each) into a kWbStages-deep shared-memory ring; consumers copy a
-// block into registers (thread t: row t/16 + 16i, 16-byte column t%16,
-// i = 0..7), free the stage at once, reduce the block amax and cast from
-// registers, so loads of the next blocks overlap the cast of this one.
+// K4: one persistent CTA per SM: a TMA producer warp and two consumer groups
+// of 8 warps.  The producer streams whole 128x128 weight blocks (32 KB of
+// FP16/BF16, one 2-D TMA box each) into a kWbStages-deep shared-memory ring;
+// the CTA's i-th block goes to consumer group i % 2, so the two groups work
+// on alternate blocks at once.  A group copies its block into registers
+// (thread t: row t/16 + 16i, 16-byte column t%16, i = 0..7), frees the stage
+// at once, reduces the block amax and casts from registers, so loads of the
+// next blocks overlap the cast of this one.  One CTA per SM keeps the block
+// count of the busiest SM at ceil(blocks / SMs).
 // Waits are bounded; a consumer that gives up raises a shared abort flag that
-// every consumer reads after the same named barrier, so they leave together.
-constexpr int kWbStages = 3;
+// every consumer of its group reads after the group's named barrier, so they
+// leave together.
+constexpr int kWbStages = 6;
+constexpr int kWbGroups = 2;
+constexpr int kWbThreads = 32 * (8 * kWbGroups + 1);
 constexpr int kWbBlockBytes = 128 * 128 * 2;
 constexpr int kWbSmemBytes = 1024 + kWbStages * kWbBlockBytes + 256;
 
 template <int DT>
-__global__ void __launch_bounds__(288, 2)
+__global__ void __launch_bounds__(kWbThreads, 1)
     quant_weight_block_tma_kernel(const __grid_constant__ CUtensorMap tmap_w, uint2* __restrict__ q,
                                   float* __restrict__ sb, int N, int KB, int num_blocks,
                                   unsigned long long timeout_ns) {
@@ -300,12 +312,11 @@ __global__ void __launch_bounds__(288, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kWbStages * kWbBlockBytes);
   uint64_t* empty_bar = full_bar + kWbStages;
-  uint32_t* warp_max = reinterpret_cast<uint32_t*>(empty_bar + kWbStages);  // [2][8]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(warp_max + 16);
+  uint32_t* warp_max = reinterpret_cast<uint32_t*>(empty_bar + kWbStages);  // [group][2][8]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(warp_max + kWbGroups * 16);
 
-  const int t = threadIdx.x;
-  const int warp = t >> 5, lane = t & 31;
-  if (t == 0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
     for (int s = 0; s < kWbStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 8);
@@ -314,8 +325,10 @@ __global__ void __launch_bounds__(288, 2)
     ptx::fence_mbar_init();
   }
   __syncthreads();
+  ptx::griddep_wait();  // the previous kernel's writes are visible from here on
+  ptx::griddep_launch();
 
-  if (warp == 8) {
+  if (warp == 8 * kWbGroups) {
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmap_w);
       uint32_t it = 0;
@@ -335,9 +348,14 @@ __global__ void __launch_bounds__(288, 2)
         if (!ptx::mbar_wait_bounded(&full_bar[j % kWbStages], (j / kWbStages) & 1, timeout_ns)) record_quant_error();
     }
   } else {
+    const int grp = warp >> 3;                 // consumer group
+    const int gw = warp & 7;                   // warp within the group
+    const int t = threadIdx.x & 255;           // thread within the group
+    uint32_t* gmax = warp_max + grp * 16;
     const int64_t row_vec = static_cast<int64_t>(KB) * 16;
-    uint32_t it = 0;
-    for (int b = blockIdx.x; b < num_blocks; b += gridDim.x, ++it) {
+    uint32_t k = 0;                            // blocks this group has done
+    for (uint32_t it = grp; blockIdx.x + static_cast<int64_t>(it) * gridDim.x < num_blocks; it += kWbGroups, ++k) {
+      const int b = static_cast<int>(blockIdx.x + static_cast<int64_t>(it) * gridDim.x);
       const int s = it % kWbStages;
       const int bi = b / KB, bj = b - (b / KB) * KB;
       const bool ok = ptx::mbar_wait_bounded(&full_bar[s], (it / kWbStages) & 1, timeout_ns);
@@ -357,12 +375,12 @@ __global__ void __launch_bounds__(288, 2)
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-      if (lane == 0) warp_max[(it & 1) * 8 + warp] = a;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (lane == 0) gmax[(k & 1) * 8 + gw] = a;
+      ptx::named_bar_sync(1 + grp, 256);
       if (*abort_flag) break;
-      a = warp_max[(it & 1) * 8];
+      a = gmax[(k & 1) * 8];
 #pragma unroll
-      for (int i = 1; i < 8; ++i) a = max(a, warp_max[(it & 1) * 8 + i]);
+      for (int i = 1; i < 8; ++i) a = max(a, gmax[(k & 1) * 8 + i]);
       const UnitScale us(mag_to_float<DT>(a));
       const int col = bj * 16 + (t & 15);
       if (__builtin_expect(!us.exact_div, 1)) {
@@ -394,6 +412,8 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, 
                                                    const uint16_t* __restrict__ tail, int ntail,
                                                    unsigned int* __restrict__ amax_word) {
   __shared__ uint32_t warp_max[8];
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   uint32_t a = 0;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -420,6 +440,8 @@ __global__ void __launch_bounds__(256) cast_per_tensor_kernel(const uint4* __res
                                                               const uint16_t* __restrict__ tail, int ntail,
                                                               uint2* __restrict__ q, uint8_t* __restrict__ q_tail,
                                                               const unsigned int* __restrict__ amax_word) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const UnitScale us(__uint_as_float(*amax_word));
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -434,6 +456,8 @@ __global__ void __launch_bounds__(256) cast_per_tensor_kernel(const uint4* __res
 
 // Turns the finished amax (bits in *word) into the stored scale, in place.
 __global__ void finalize_scale_kernel(unsigned int* word) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const float amax = __uint_as_float(*word);
   const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
   *reinterpret_cast<float*>(word) = s;

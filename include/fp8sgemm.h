@@ -125,8 +125,9 @@ FP8S_API fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const u
  * any device use output tiles of 128 x bn and split each tile's K range over
  * `splits` CTAs of a thread-block cluster, or (pair != 0, splits == 1, bn >=
  * 64) tiles of 256 x bn shared by a pair of CTAs, instead of the library's
- * own choice.  bn in {32, 64, 128, 256}; splits in {1, 2, 4, 8}.  With
- * splits > 1 every cluster must own a single output tile; a later call whose
+ * own choice.  bn in {32, 64, 128, 192, 256}; splits in {1, 2, 4, 8}, with
+ * splits > 1 only for bn <= 192.  With splits > 1 every cluster must own a
+ * single output tile; a later call whose
  * K has fewer 128-wide blocks than `splits`, or with more 128 x bn output
  * tiles than the device can hold clusters of `splits` CTAs at once, fails
  * with FP8S_ERR_SHAPE.  bn = 0 restores the automatic choice.

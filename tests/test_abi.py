@@ -101,10 +101,13 @@ def test_oracle_is_not_linked_into_the_library(lib):
 def test_gemm_override_argument_checks(lib):
     assert lib.fp8s_gemm_override(3, 1, 0) == 2
     assert lib.fp8s_gemm_override(256, 16, 0) == 2
-    assert lib.fp8s_gemm_override(256, 8, 0) == 0
+    assert lib.fp8s_gemm_override(256, 8, 0) == 2     # split-K only up to bn = 192
+    assert lib.fp8s_gemm_override(192, 8, 0) == 0
     assert lib.fp8s_gemm_override(128, 3, 0) == 2
     assert lib.fp8s_gemm_override(128, 4, 0) == 0
     assert lib.fp8s_gemm_override(128, 2, 1) == 2     # a pair does not also split K
     assert lib.fp8s_gemm_override(32, 1, 1) == 2      # a pair needs bn >= 64
     assert lib.fp8s_gemm_override(256, 1, 1) == 0
+    assert lib.fp8s_gemm_override(192, 4, 0) == 0
+    assert lib.fp8s_gemm_override(96, 1, 0) == 2
     assert lib.fp8s_gemm_override(0, 0, 0) == 0
