@@ -23,7 +23,7 @@ from ._lib import (FP8S_BF16, FP8S_F16, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_TENSOR,
 
 __all__ = [
     "fp8_quantize_per_tensor", "fp8_quantize_token_group", "fp8_quantize_weight_block", "fp8_gemm_scaled",
-    "fp8s_device_error", "fp8s_version", "fp8s_gemm_override", "Fp8sError", "status_string", "load", "LIB_PATH",
+    "fp8s_device_error", "fp8s_version", "fp8s_gemm_override", "fp8s_gemm_plan", "Fp8sError", "status_string", "load", "LIB_PATH",
     "FP8S_F16", "FP8S_BF16", "FP8S_SCALE_PER_TENSOR", "FP8S_SCALE_BLOCK",
 ]
 
@@ -113,6 +113,14 @@ def fp8s_device_error(stream=None):
 def fp8s_gemm_override(bn=0, splits=1, pair=False):
     """Force the GEMM tile width, split-K factor or CTA-pair tiles (bn=0: automatic choice)."""
     check(load().fp8s_gemm_override(int(bn), int(splits), int(bool(pair))), "fp8s_gemm_override")
+
+
+def fp8s_gemm_plan(M, N, K, mode="block", sms=148):
+    """(bn, splits, pair) that fp8_gemm_scaled picks for this shape (host only)."""
+    bn, sp, pr = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    check(load().fp8s_gemm_plan(int(M), int(N), int(K), _MODE[mode], int(sms), ctypes.byref(bn), ctypes.byref(sp),
+                                ctypes.byref(pr)), "fp8s_gemm_plan")
+    return bn.value, sp.value, bool(pr.value)
 
 
 def fp8s_version():

@@ -32,6 +32,7 @@ SIGNATURES = {
     "fp8s_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "fp8s_version": (_I, []),
     "fp8s_gemm_override": (_I, [_I, _I, _I]),
+    "fp8s_gemm_plan": (_I, [_I64, _I64, _I64, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
 }
 
 _lib = None

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -333,34 +334,64 @@ fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const 
   }
 }
 
-// Relative tensor-pipe efficiency of one 128 x BN x 128 K block, measured on
-// the B300 for each tile width (narrow tiles are bound by shared-memory
-// operand traffic, not by the MMA).
-double tile_eff(int bn) { return bn == 256 ? 1.0 : bn == 128 ? 0.62 : bn == 64 ? 0.40 : 0.25; }
+// Time model for choosing the tile width, split-K factor and CTA pairing,
+// in microseconds, with constants measured on the B300 (sweeps of every
+// configuration over the workloads' shapes, inputs rotated past L2):
+//  - a CTA's time per 128-wide K block of its tile is the larger of the
+//    tensor-pipe-and-epilogue time (per width, mode and pairing; narrow
+//    tiles are bound by shared-memory operand traffic, block mode by the
+//    per-K-block promotion in the epilogue) and the time to stream the
+//    block's operands at ~85 GB/s per SM;
+//  - the whole grid is bound below by the L2 -> SM traffic at ~10.5 TB/s
+//    and by HBM traffic at ~6.2 TB/s;
+//  - a launch costs ~2.5 us of fixed time (prologue, first loads, tail), a
+//    split-K exchange ~4 us more and a CTA pair's start-up ~0.7 us more.
+double kb_compute_us(int bn, int mode, bool pair) {
+  if (mode == FP8S_SCALE_BLOCK) {
+    if (pair) return 1e9;  // a per-K-block hand-off across the pair stalls the MMA
+    return bn == 256 ? 0.684 : bn == 192 ? 0.5625 : bn == 128 ? 0.458 : bn == 64 ? 0.415 : 0.39;
+  }
+  if (pair) return bn == 256 ? 0.43 : bn == 192 ? 0.40 : 0.35;
+  return bn == 256 ? 0.475 : bn == 192 ? 0.40 : bn == 128 ? 0.343 : 0.33;
+}
 
-// Tile width and split: the candidate with the least estimated time.  A
-// persistent CTA's time is (waves of tiles) x (its K blocks per tile) x (the
-// cost of one K block at that width), plus a fixed part per tile (pipeline
-// fill, epilogue) and, for split-K, the partial exchange.
+double estimate_us(int64_t M, int64_t N, int64_t KB, int mode, int sms, int bn, int s, bool pair) {
+  const int64_t tile_m = pair ? 2 * kBM : kBM;
+  const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
+  const int64_t csize = pair ? 2 : s;
+  const int64_t clusters = sms / csize;
+  const int64_t waves = (tiles + clusters - 1) / clusters;
+  const int64_t nkb = (KB + s - 1) / s;
+  const double kb_bytes = 16384.0 + (pair ? bn * 64.0 : bn * 128.0);  // per CTA per K block
+  const double kb_us = std::max(kb_compute_us(bn, mode, pair), kb_bytes / 85e3);
+  double t = static_cast<double>(waves) * static_cast<double>(nkb) * kb_us;
+  const double l2_bytes = static_cast<double>(tiles) * csize * static_cast<double>(nkb) * kb_bytes;
+  const double hbm_bytes = static_cast<double>(M) * KB * 128 + static_cast<double>(N) * KB * 128 + 2.0 * M * N;
+  t = std::max(t, std::max(l2_bytes / 10.5e6, hbm_bytes / 6.2e6));
+  return t + 2.5 + (s > 1 ? 4.0 : 0.0) + (pair ? 0.7 : 0.0);  // a pair also waits on a cluster barrier to start
+}
+
 GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms) {
   GemmChoice best;
-  double best_cost = 1e300;
-  const int bns[] = {256, 128, 64, 32};
+  double best_t = 1e300;
+  const int bns[] = {256, 192, 128, 64, 32};
   const int64_t tm = (M + kBM - 1) / kBM;
   for (int bn : bns) {
     for (int s = 1; s <= 8; s *= 2) {
       if (s > KB || (s > 1 && bn > 192)) continue;
       const int64_t tiles = tm * ((N + bn - 1) / bn);
-      const int64_t clusters = sms / s;
-      if (s > 1 && tiles > clusters * 7 / 8) continue;  // split-K needs one tile per cluster (with slack for GPC packing)
-      const int64_t waves = (tiles + clusters - 1) / clusters;
-      const int64_t kb = (KB + s - 1) / s;
-      double cost = static_cast<double>(waves) * (static_cast<double>(kb) * bn / tile_eff(bn) + 64.0);
-      if (s > 1) cost += static_cast<double>(waves) * (32.0 + 0.25 * bn * s);
-      if (cost < best_cost * 0.999) {
-        best_cost = cost;
-        best.bn = bn;
-        best.splits = s;
+      // split-K needs one tile per cluster (with slack for GPC packing)
+      if (s > 1 && tiles > (sms / s) * 7 / 8) continue;
+      for (int pr = 0; pr < 2; ++pr) {
+        const bool pair = pr != 0;
+        if (pair && (s > 1 || bn < 64 || M <= kBM)) continue;
+        const double t = estimate_us(M, N, KB, mode, sms, bn, s, pair);
+        if (t < best_t * 0.999) {
+          best_t = t;
+          best.bn = bn;
+          best.splits = s;
+          best.pair = pair;
+        }
       }
     }
   }
@@ -510,6 +541,19 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
     r = run(ch);
   }
   return r;
+}
+
+fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode, int sms, int* bn, int* splits,
+                           int* pair) {
+  if (mode != FP8S_SCALE_PER_TENSOR && mode != FP8S_SCALE_BLOCK) return FP8S_ERR_DTYPE;
+  if (!bn || !splits || !pair) return FP8S_ERR_NULL;
+  if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || sms < 1) return FP8S_ERR_SHAPE;
+  if (mode == FP8S_SCALE_BLOCK && K % 128 != 0) return FP8S_ERR_SHAPE;
+  const GemmChoice ch = choose_gemm(M, N, (K + kBK - 1) / kBK, mode, sms);
+  *bn = ch.bn;
+  *splits = ch.splits;
+  *pair = ch.pair ? 1 : 0;
+  return FP8S_OK;
 }
 
 fp8s_status fp8s_gemm_override(int bn, int splits, int pair) {

@@ -89,21 +89,19 @@ struct GemmCfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 192 || BN == 256, "BN");
   static_assert(!(SPLIT && PAIR), "a CTA pair does not also split K");
   static_assert(!PAIR || BN >= 64, "a CTA pair holds at least 32 rows of B each");
-  // Block mode keeps the tile's FP32 accumulators in the epilogue threads'
-  // registers: BN = 256 uses four epilogue warpgroups (64 columns each);
-  // BN = 192 uses six (32 columns each, so one TMEM load covers a thread's
-  // share of a K block).
-  static constexpr int kEpiWarps = MODE != kModeBlock ? 8 : BN == 256 ? 16 : BN == 192 ? 24 : 8;
+  // Block mode keeps 64 FP32 accumulators per epilogue thread: BN = 192 and
+  // 256 need three and four epilogue warpgroups.
+  static constexpr int kEpiWarps = MODE != kModeBlock ? 8 : BN == 256 ? 16 : BN == 192 ? 12 : 8;
   static constexpr int kEpiWG = kEpiWarps / 4;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kThreads = 128 + kEpiThreads;
   static constexpr bool kLowReg = kEpiWarps == 16;  // 640 threads: at most 96 registers each
-  // Block mode with 16 or 24 epilogue warps (at most 96 or 72 registers a
-  // thread) reads a K block's partial 16 columns per wait, so only one chunk
-  // is staged next to the accumulators.
+  // Block mode with 12 or 16 epilogue warps (at most 128 or 96 registers a
+  // thread) reads a K block's partial 32 or 16 columns per wait, so only one
+  // chunk is staged next to the 64 accumulators.
   static constexpr bool kSeqChunks = MODE == kModeBlock && kEpiWarps >= 12;
   // Columns of a K block's partial loaded per wait.
-  static constexpr int kSeqLoadCols = 16;
+  static constexpr int kSeqLoadCols = kLowReg ? 16 : 32;
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;   // output rows per (pair) tile
   static constexpr int kBRows = PAIR ? BN / 2 : BN;     // rows of B this CTA loads
   static constexpr int kABytes = kBM * kBK;
@@ -130,7 +128,7 @@ struct GemmCfg {
   static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                   : kTmemCols <= 256 ? 256 : 512;  // allocations are powers of two
   static constexpr int kColsPerThread = BN / kEpiWG;
-  static constexpr int kChunk = (kLowReg || kEpiWarps == 24) ? 16 : (kColsPerThread < 32 ? kColsPerThread : 32);
+  static constexpr int kChunk = kLowReg ? 16 : (kColsPerThread < 32 ? kColsPerThread : 32);
   static_assert(kColsPerThread % kChunk == 0, "chunks tile a thread's columns");
   // Block mode: K blocks the epilogue takes per TMEM hand-off (one
   // tcgen05.wait::ld per batch), capped by registers and by half the buffers.

@@ -15,12 +15,17 @@
 //  * fl32(x / s) is computed without a per-element divide.  With y the
 //    correctly rounded reciprocal of s (computed once per unit), q0 = x*y is
 //    refined twice by the remainder r = x - s*q (exact via FMA) and
-//    q' = q + r*y (two elements at a time with the packed .f32x2 FMA).  The first refinement leaves q within one ulp of x/s; the
-//    second then returns the correctly rounded quotient (Markstein, "IA-64
-//    and Elementary Functions", theorem on division by reciprocal
-//    refinement).  Zeros keep the sign of x (x/s with s > 0, so -0 stays
-//    -0).  Units whose scale is tiny (s < 2^-90, possible only for BF16
-//    inputs below about 2^-81) use the IEEE divide __fdiv_rn.
+//    q' = q + r*y (two elements at a time with the packed .f32x2 FMA).  The
+//    first refinement leaves q within one ulp of x/s; the second then
+//    returns the correctly rounded quotient (Markstein, "IA-64 and
+//    Elementary Functions", theorem on division by reciprocal refinement).
+//    The only value this sequence gets wrong in sign is an input of -0 (the
+//    sum of the two zero terms rounds to +0), and the E4M3 code of -0/s is
+//    0x80: so the input's sign bit is OR-ed into every code, which changes
+//    nothing else (a negative non-zero quotient already has its sign bit,
+//    including one that rounds to zero).  Units whose scale is tiny
+//    (s < 2^-90, possible only for BF16 inputs below about 2^-81) use the
+//    IEEE divide __fdiv_rn.
 //  * the E4M3 rounding is the hardware cvt.rn.satfinite.e4m3x2.f32.
 #pragma once
 
@@ -97,56 +102,77 @@ struct UnitScale {
     return q;
   }
 
-  // The same two steps on a pair (x = {lo, hi}, nx = {-lo, -hi}); q - r'*y
-  // is written fma(r', -y, q), which is the same product and the same rounding.
-  __device__ __forceinline__ uint64_t div_fast2(uint64_t x, uint64_t nx) const {
-    const uint64_t ss = ptx::f2_pack(s, s), yy = ptx::f2_pack(y, y), nyy = ptx::f2_pack(-y, -y);
-    uint64_t q = ptx::f2_mul(x, yy);
-    uint64_t r = ptx::f2_fma(ss, q, nx);
-    q = ptx::f2_fma(r, nyy, q);
-    r = ptx::f2_fma(ss, q, nx);
-    q = ptx::f2_fma(r, nyy, q);
-    return q;
-  }
-
   __device__ __forceinline__ float div_exact(float x) const { return __fdiv_rn(x, s); }
 };
 
-// Two packed 16-bit inputs -> {x_lo, x_hi} and {-x_lo, -x_hi} as FP32 pairs.
+// Two packed 16-bit inputs -> {x_lo, x_hi} as an FP32 pair.  Exact.
 template <int DT>
-__device__ __forceinline__ void unpack2_pm(uint32_t w, uint64_t& x, uint64_t& nx) {
+__device__ __forceinline__ uint64_t unpack2_f2(uint32_t w) {
   if constexpr (DT == kInF16) {
     const float2 f = unpack2<DT>(w);
-    x = ptx::f2_pack(f.x, f.y);
-    nx = ptx::f2_pack(-f.x, -f.y);
+    return ptx::f2_pack(f.x, f.y);
   } else {
-    const uint32_t lo = w << 16, hi = w & 0xFFFF0000u;
-    x = ptx::f2_pack(__uint_as_float(lo), __uint_as_float(hi));
-    nx = ptx::f2_pack(__uint_as_float(lo ^ 0x80000000u), __uint_as_float(hi ^ 0x80000000u));
+    return ptx::f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
   }
 }
 
-// Two packed 16-bit inputs -> two E4M3 bytes (low input in the low byte).
+// The unit's constants for the packed refinement: {-s, -s} and {y, y}.
+struct UnitPair {
+  uint64_t nss, yy;
+  __device__ __forceinline__ explicit UnitPair(const UnitScale& us)
+      : nss(ptx::f2_pack(-us.s, -us.s)), yy(ptx::f2_pack(us.y, us.y)) {}
+};
+
+// Two packed 16-bit inputs -> two E4M3 bytes (low input in the low byte),
+// without the sign of a -0 input (see quant4).
+template <int DT>
+__device__ __forceinline__ uint32_t quant2_fast(uint32_t w, const UnitPair& k) {
+  const uint64_t x = unpack2_f2<DT>(w);
+  uint64_t q = ptx::f2_mul(x, k.yy);
+  uint64_t r = ptx::f2_fma(k.nss, q, x);  // x - s*q, exact
+  q = ptx::f2_fma(r, k.yy, q);
+  r = ptx::f2_fma(k.nss, q, x);
+  q = ptx::f2_fma(r, k.yy, q);
+  float lo, hi;
+  ptx::f2_unpack(q, lo, hi);
+  return ptx::cvt_e4m3x2(hi, lo);
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t quant2_exact(uint32_t w, const UnitScale& us) {
+  const float2 f = unpack2<DT>(w);
+  return ptx::cvt_e4m3x2(us.div_exact(f.y), us.div_exact(f.x));
+}
+
+// Input sign bits of two packed 16-bit words, at the sign positions of the
+// four E4M3 bytes they quantize to.
+__device__ __forceinline__ uint32_t sign_bytes(uint32_t w0, uint32_t w1) {
+  return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
+}
+
+// 4 inputs (two words) -> 4 E4M3 bytes.
 template <int DT, bool kExact>
-__device__ __forceinline__ uint32_t quant2(uint32_t w, const UnitScale& us) {
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, const UnitScale& us, const UnitPair& k) {
+  uint32_t c0, c1;
   if constexpr (kExact) {
-    const float2 f = unpack2<DT>(w);
-    return ptx::cvt_e4m3x2(us.div_exact(f.y), us.div_exact(f.x));
+    c0 = quant2_exact<DT>(w0, us);
+    c1 = quant2_exact<DT>(w1, us);
   } else {
-    uint64_t x, nx;
-    unpack2_pm<DT>(w, x, nx);
-    float lo, hi;
-    ptx::f2_unpack(us.div_fast2(x, nx), lo, hi);
-    return ptx::cvt_e4m3x2(hi, lo);
+    c0 = quant2_fast<DT>(w0, k);
+    c1 = quant2_fast<DT>(w1, k);
   }
+  return __byte_perm(c0, c1, 0x5410) | sign_bytes(w0, w1);
 }
 
 // 8 input elements (one 16-byte vector) -> 8 E4M3 bytes.
 template <int DT, bool kExact>
+__device__ __forceinline__ uint2 quant8_impl(const uint4& v, const UnitScale& us, const UnitPair& k) {
+  return make_uint2(quant4<DT, kExact>(v.x, v.y, us, k), quant4<DT, kExact>(v.z, v.w, us, k));
+}
+
+template <int DT, bool kExact>
 __device__ __forceinline__ uint2 quant8_impl(const uint4& v, const UnitScale& us) {
-  const uint32_t p0 = quant2<DT, kExact>(v.x, us), p1 = quant2<DT, kExact>(v.y, us);
-  const uint32_t p2 = quant2<DT, kExact>(v.z, us), p3 = quant2<DT, kExact>(v.w, us);
-  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+  return quant8_impl<DT, kExact>(v, us, UnitPair(us));
 }
 
 // The per-unit choice of division path is made once, outside the element loop.
@@ -161,6 +187,13 @@ __device__ __forceinline__ uint8_t quant1(uint16_t h, const UnitScale& us) {
   float x = unpack2<DT>(static_cast<uint32_t>(h)).x;
   const float t = us.exact_div ? us.div_exact(x) : us.div_fast(x);
   return static_cast<uint8_t>(ptx::cvt_e4m3x2(0.0f, t) & 0xFFu);
+}
+
+// 16-byte load from this CTA's shared memory.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
 
 // Streaming 16-byte load that does not allocate in L1.
@@ -247,12 +280,13 @@ __global__ void __launch_bounds__(288, 2)
         break;
       }
       const uint32_t gw = c * kTgChunkGroups + warp * GPW;  // first group of this warp
-      const uint4* tile = reinterpret_cast<const uint4*>(smem + s * kTgChunkBytes) + warp * GPW * 16;
+      const uint32_t tile = ptx::smem_u32(smem + s * kTgChunkBytes) + static_cast<uint32_t>(warp * GPW * 256);
       uint4 v[GPW / 2];
       uint32_t mine = 0;  // lanes 0..GPW-1: amax bits of group gw + lane
 #pragma unroll
       for (int j = 0; j < GPW / 2; ++j) {
-        v[j] = tile[(2 * j + half) * 16 + hl];  // groups past the end hold stale data; never stored
+        // groups past the end hold stale data; never stored
+        v[j] = lds128(tile + static_cast<uint32_t>(((2 * j + half) * 16 + hl) * 16));
         uint32_t a = amax_bits8(v[j]);
         a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
         a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
@@ -271,13 +305,26 @@ __global__ void __launch_bounds__(288, 2)
         const uint32_t m = my_group / G;
         sa[static_cast<uint64_t>(my_group - m * G) * M + m] = own.s;
       }
+      // Warp-uniform choices, made once per chunk: every group present, and
+      // no group needing the IEEE divide (then no per-group branches).
+      const bool whole = gw + GPW <= num_groups;
+      const bool any_exact = __any_sync(0xFFFFFFFFu, lane < GPW && own.exact_div);
+      uint2* qw = q + static_cast<uint64_t>(gw) * 16 + hl;
+      if (whole && !any_exact) {
 #pragma unroll
-      for (int j = 0; j < GPW / 2; ++j) {
-        const int src = 2 * j + half;
-        const UnitScale us(__shfl_sync(0xFFFFFFFFu, own.s, src), __shfl_sync(0xFFFFFFFFu, own.y, src),
-                           __shfl_sync(0xFFFFFFFFu, own.exact_div ? 1 : 0, src) != 0);
-        const uint32_t g = gw + src;
-        if (g < num_groups) q[static_cast<uint64_t>(g) * 16 + hl] = quant8<DT>(v[j], us);
+        for (int j = 0; j < GPW / 2; ++j) {
+          const int src = 2 * j + half;
+          const UnitScale us(__shfl_sync(0xFFFFFFFFu, own.s, src), __shfl_sync(0xFFFFFFFFu, own.y, src), false);
+          qw[src * 16] = quant8_impl<DT, false>(v[j], us);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < GPW / 2; ++j) {
+          const int src = 2 * j + half;
+          const UnitScale us(__shfl_sync(0xFFFFFFFFu, own.s, src), __shfl_sync(0xFFFFFFFFu, own.y, src),
+                             __shfl_sync(0xFFFFFFFFu, own.exact_div ? 1 : 0, src) != 0);
+          if (gw + src < num_groups) qw[src * 16] = quant8<DT>(v[j], us);
+        }
       }
     }
   }
@@ -361,10 +408,10 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       const bool ok = ptx::mbar_wait_bounded(&full_bar[s], (it / kWbStages) & 1, timeout_ns);
       uint4 v[8];
       uint32_t a = 0;
-      const uint4* tile = reinterpret_cast<const uint4*>(smem + s * kWbBlockBytes);
+      const uint32_t tile = ptx::smem_u32(smem + s * kWbBlockBytes) + static_cast<uint32_t>(t * 16);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        v[i] = tile[t + 256 * i];
+        v[i] = lds128(tile + static_cast<uint32_t>(i * 256 * 16));
         a = max(a, amax_bits8(v[i]));
       }
       __syncwarp();
@@ -382,19 +429,21 @@ __global__ void __launch_bounds__(kWbThreads, 1)
 #pragma unroll
       for (int i = 1; i < 8; ++i) a = max(a, gmax[(k & 1) * 8 + i]);
       const UnitScale us(mag_to_float<DT>(a));
-      const int col = bj * 16 + (t & 15);
-      if (__builtin_expect(!us.exact_div, 1)) {
+      const UnitPair k(us);
+      const int r0 = bi * 128 + (t >> 4);
+      uint2* qrow = q + static_cast<int64_t>(r0) * row_vec + bj * 16 + (t & 15);
+      const int64_t step = 16 * row_vec;  // 16 rows down
+      if (__builtin_expect(!us.exact_div && bi * 128 + 128 <= N, 1)) {  // whole block, fast divide
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = bi * 128 + (t >> 4) + 16 * i;
-          if (r < N) q[r * row_vec + col] = quant8_impl<DT, false>(v[i], us);
-        }
+        for (int i = 0; i < 8; ++i) qrow[i * step] = quant8_impl<DT, false>(v[i], us, k);
+      } else if (!us.exact_div) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (r0 + 16 * i < N) qrow[i * step] = quant8_impl<DT, false>(v[i], us, k);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = bi * 128 + (t >> 4) + 16 * i;
-          if (r < N) q[r * row_vec + col] = quant8_impl<DT, true>(v[i], us);
-        }
+        for (int i = 0; i < 8; ++i)
+          if (r0 + 16 * i < N) qrow[i * step] = quant8_impl<DT, true>(v[i], us, k);
       }
       if (t == 0) sb[static_cast<int64_t>(bi) * KB + bj] = us.s;
     }

@@ -136,6 +136,19 @@ FP8S_API fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const u
  */
 FP8S_API fp8s_status fp8s_gemm_override(int bn, int splits, int pair);
 
+/*
+ * fp8s_gemm_plan -- the tile configuration fp8_gemm_scaled picks for a
+ * shape on a device with `sms` streaming multiprocessors (148 on the B300),
+ * from a time model whose constants were measured on the B300: *bn (output
+ * tile 128 x bn, or 256 x bn when *pair), *splits (CTAs of a cluster sharing
+ * one tile's K range; 1 = none) and *pair (1 when two CTAs share a 256-row
+ * tile through tcgen05 cta_group::2).  Host-only and side-effect free; no
+ * GPU is needed.  Same shape rules and status codes as fp8_gemm_scaled.  (At
+ * run time a split that the device cannot hold falls back to splits = 1.)
+ */
+FP8S_API fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode, int sms, int* bn,
+                                    int* splits, int* pair);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 FP8S_API const char* fp8s_status_string(fp8s_status status);
 

@@ -111,3 +111,35 @@ def test_gemm_override_argument_checks(lib):
     assert lib.fp8s_gemm_override(192, 4, 0) == 0
     assert lib.fp8s_gemm_override(96, 1, 0) == 2
     assert lib.fp8s_gemm_override(0, 0, 0) == 0
+
+
+def plan(lib, M, N, K, mode):
+    bn, sp, pr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    st = lib.fp8s_gemm_plan(M, N, K, mode, 148, ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(pr))
+    assert st == 0
+    return bn.value, sp.value, pr.value
+
+
+def test_gemm_plan_matches_measured_choices(lib):
+    """The tile choice for the workloads' shapes is the configuration that
+    measured fastest on the B300 in sweeps of every configuration."""
+    BLOCK, PT = 1, 0
+    assert plan(lib, 128, 4096, 4096, BLOCK) == (128, 4, 0)      # decode: split K over clusters of 4
+    assert plan(lib, 128, 4096, 11008, BLOCK) == (128, 4, 0)
+    assert plan(lib, 128, 22016, 4096, BLOCK) == (192, 1, 0)     # 115 tiles already fill the GPU
+    assert plan(lib, 512, 2560, 2048, BLOCK) == (128, 1, 0)
+    assert plan(lib, 4096, 22016, 4096, BLOCK) == (256, 1, 0)    # large: widest single-CTA tile
+    assert plan(lib, 16384, 8192, 8192, PT) == (256, 1, 1)       # large per-tensor: CTA pairs
+    assert plan(lib, 512, 2048, 2048, PT)[2] == 0                # no pair when it cannot pay for its start-up
+    bn, sp, pr = plan(lib, 64, 64, 128, PT)
+    assert sp == 1 and pr == 0
+
+
+def test_gemm_plan_argument_checks(lib):
+    bn, sp, pr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    args = (ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(pr))
+    assert lib.fp8s_gemm_plan(128, 128, 100, 1, 148, *args) == 2   # block mode needs K % 128 == 0
+    assert lib.fp8s_gemm_plan(0, 128, 128, 1, 148, *args) == 2
+    assert lib.fp8s_gemm_plan(128, 128, 128, 5, 148, *args) == 4
+    assert lib.fp8s_gemm_plan(128, 128, 128, 1, 0, *args) == 2
+    assert lib.fp8s_gemm_plan(128, 128, 128, 1, 148, None, *args[1:]) == 1
