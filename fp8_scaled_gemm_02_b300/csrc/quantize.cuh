@@ -341,9 +341,9 @@ __global__ void __launch_bounds__(288, 2)
 // at once, reduces the block amax and casts from registers, so loads of the
 // next blocks overlap the cast of this one.  One CTA per SM keeps the block
 // count of the busiest SM at ceil(blocks / SMs).
-// Waits are bounded; a consumer that gives up raises a shared abort flag that
-// every consumer of its group reads after the group's named barrier, so they
-// leave together.
+// Waits are bounded.  The group's named barrier also ORs its threads' failed
+// waits, so every warp of a group takes the same decision to leave; the
+// producer gives up on its own.
 constexpr int kWbStages = 6;
 constexpr int kWbGroups = 2;
 constexpr int kWbThreads = 32 * (8 * kWbGroups + 1);
@@ -360,7 +360,6 @@ __global__ void __launch_bounds__(kWbThreads, 1)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kWbStages * kWbBlockBytes);
   uint64_t* empty_bar = full_bar + kWbStages;
   uint32_t* warp_max = reinterpret_cast<uint32_t*>(empty_bar + kWbStages);  // [group][2][8]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(warp_max + kWbGroups * 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -368,7 +367,6 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 8);
     }
-    *abort_flag = 0;
     ptx::fence_mbar_init();
   }
   __syncthreads();
@@ -416,15 +414,12 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);
-      if (!ok) {
-        record_quant_error();
-        *abort_flag = 1;
-      }
+      if (!ok) record_quant_error();
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
       if (lane == 0) gmax[(k & 1) * 8 + gw] = a;
-      ptx::named_bar_sync(1 + grp, 256);
-      if (*abort_flag) break;
+      // the barrier ORs the group's failed waits: the whole group leaves together
+      if (ptx::named_bar_sync_or(1 + grp, 256, !ok)) break;
       a = gmax[(k & 1) * 8];
 #pragma unroll
       for (int i = 1; i < 8; ++i) a = max(a, gmax[(k & 1) * 8 + i]);
