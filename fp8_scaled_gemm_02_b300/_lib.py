@@ -11,6 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfp8sgemm.so")
 
 FP8S_OK = 0
+FP8S_ERR_CUDA = 5
 STATUS_NAMES = {
     0: "FP8S_OK", 1: "FP8S_ERR_NULL", 2: "FP8S_ERR_SHAPE", 3: "FP8S_ERR_ALIGN", 4: "FP8S_ERR_DTYPE",
     5: "FP8S_ERR_CUDA", 6: "FP8S_ERR_DEVICE_TIMEOUT", 7: "FP8S_ERR_UNSUPPORTED_DEVICE",
@@ -29,6 +30,7 @@ SIGNATURES = {
     "fp8_quantize_weight_block": (_I, [_P, _I, _I64, _I64, _P, _P, _P]),
     "fp8_gemm_scaled": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P]),
     "fp8s_status_string": (ctypes.c_char_p, [_I]),
+    "fp8s_last_cuda_error": (ctypes.c_char_p, []),
     "fp8s_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "fp8s_version": (_I, []),
     "fp8s_gemm_override": (_I, [_I, _I, _I]),
@@ -42,7 +44,10 @@ class Fp8sError(RuntimeError):
     def __init__(self, status, where=""):
         self.status = int(status)
         name = STATUS_NAMES.get(self.status, str(status))
-        super().__init__(f"{where}: {name} ({status_string(self.status)})")
+        detail = status_string(self.status)
+        if self.status == FP8S_ERR_CUDA:
+            detail += f": {load().fp8s_last_cuda_error().decode()}"
+        super().__init__(f"{where}: {name} ({detail})")
 
 
 def load():

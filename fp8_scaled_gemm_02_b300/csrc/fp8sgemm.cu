@@ -28,6 +28,20 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per mbarrie
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(fp8s_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Text behind the calling thread's latest FP8S_ERR_CUDA (fp8s_last_cuda_error).
+thread_local const char* t_cuda_msg = "";
+
+fp8s_status cuda_fail(const char* msg) {
+  t_cuda_msg = msg;
+  return FP8S_ERR_CUDA;
+}
+
+// Reports a runtime error (and clears it from cudaGetLastError).
+fp8s_status cuda_fail(cudaError_t e) {
+  cudaGetLastError();
+  return cuda_fail(cudaGetErrorString(e));
+}
+
 // ---------------------------------------------------------------- device
 struct DeviceInfo {
   bool ok = false;
@@ -41,10 +55,7 @@ std::mutex g_dev_mu;
 
 fp8s_status current_device(int* dev_out, DeviceInfo* info_out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8S_ERR_CUDA;
-  }
+  if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return FP8S_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
@@ -53,8 +64,7 @@ fp8s_status current_device(int* dev_out, DeviceInfo* info_out) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      cudaGetLastError();
-      return FP8S_ERR_CUDA;
+      return cuda_fail(cudaGetLastError());
     }
     d.ok = (major == 10 && minor == 3);
     d.sms = sms;
@@ -68,7 +78,7 @@ fp8s_status current_device(int* dev_out, DeviceInfo* info_out) {
 
 fp8s_status launch_status() {
   cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? FP8S_OK : FP8S_ERR_CUDA;
+  return e == cudaSuccess ? FP8S_OK : cuda_fail(cudaGetErrorString(e));
 }
 
 // ------------------------------------------------------ TMA descriptors
@@ -126,7 +136,7 @@ fp8s_status tensor_map_2d(const void* ptr, int64_t rows, int64_t cols, int elem_
     }
   }
   auto fn = encode_fn();
-  if (!fn) return FP8S_ERR_CUDA;
+  if (!fn) return cuda_fail("cuTensorMapEncodeTiled is not available from the driver");
   CUtensorMap m;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * elem_bytes)};
@@ -136,7 +146,7 @@ fp8s_status tensor_map_2d(const void* ptr, int64_t rows, int64_t cols, int elem_
   CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return FP8S_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return cuda_fail("cuTensorMapEncodeTiled rejected the tensor map");
   {
     std::lock_guard<std::mutex> lk(g_maps_mu);
     if (g_maps.size() > 4096) g_maps.clear();
@@ -178,10 +188,8 @@ fp8s_status launch_ex(void (*kern)(KArgs...), unsigned grid, unsigned block, siz
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8S_ERR_CUDA;
-  }
+  if (const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...); e != cudaSuccess)
+    return cuda_fail(e);
   return FP8S_OK;
 }
 
@@ -203,12 +211,13 @@ fp8s_status launch_token_group_gpw(const void* x, int64_t M, int64_t G, uint8_t*
                                    const DeviceInfo& info) {
   static bool attr_done[kMaxDevices] = {};
   auto kern = quant_token_group_kernel<DT, GPW>;
-  if (fp8s_status s = ensure_smem_attr(kern, kTgSmemBytes, attr_done)) return s;
+  constexpr int kSmem = tg_smem_bytes(GPW);
+  if (fp8s_status s = ensure_smem_attr(kern, kSmem, attr_done)) return s;
   const int64_t groups = M * G;
   const int64_t chunks = (groups + 8 * GPW - 1) / (8 * GPW);
   const int64_t cap = 2LL * info.sms;
   const unsigned grid = static_cast<unsigned>(chunks < cap ? chunks : cap);
-  return launch_ex(kern, grid, 288, kTgSmemBytes, st, 1, static_cast<const uint8_t*>(x), reinterpret_cast<uint2*>(q), sa,
+  return launch_ex(kern, grid, 288, kSmem, st, 1, static_cast<const uint8_t*>(x), reinterpret_cast<uint2*>(q), sa,
                    static_cast<uint32_t>(M), static_cast<uint32_t>(G), static_cast<uint32_t>(groups), kWaitTimeoutNs);
 }
 
@@ -299,8 +308,10 @@ int max_active_clusters(KernelT kern, int threads, int smem, int splits, int dev
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+  const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  if (e != cudaSuccess || n < 1) {
     cudaGetLastError();
+    t_cuda_msg = e != cudaSuccess ? cudaGetErrorString(e) : "no thread-block cluster of this kernel fits on the device";
     n = 0;
   }
   std::lock_guard<std::mutex> lk(mu);
@@ -317,7 +328,7 @@ fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const 
   if (fp8s_status s = ensure_smem_attr(kern, Cfg::kSmemBytes, attr_set)) return s;
   if constexpr (PAIR) {
     const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, 2, dev, info.sms);
-    if (cmax < 1) return FP8S_ERR_CUDA;
+    if (cmax < 1) return cuda_fail("no thread-block cluster of this kernel fits on the device");
     const int clusters = p.num_tiles < cmax ? p.num_tiles : cmax;
     return launch_ex(kern, static_cast<unsigned>(clusters * 2), Cfg::kThreads, Cfg::kSmemBytes, st, 2, ma, mb, p);
   } else if constexpr (!SPLIT) {
@@ -325,7 +336,7 @@ fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const 
     return launch_ex(kern, static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, st, 1, ma, mb, p);
   } else {
     const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, splits, dev, info.sms);
-    if (cmax < 1) return FP8S_ERR_CUDA;
+    if (cmax < 1) return cuda_fail("no thread-block cluster of this kernel fits on the device");
     // one tile per cluster: the kernel stages its split-K partials in the
     // operand ring, which only drains for good after a cluster's last tile
     if (p.num_tiles > cmax) return FP8S_ERR_SHAPE;
@@ -589,20 +600,18 @@ const char* fp8s_status_string(fp8s_status status) {
 }
 
 fp8s_status fp8s_device_error(fp8s_stream_t stream, int* where) {
-  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8S_ERR_CUDA;
-  }
+  if (const cudaError_t e = cudaStreamSynchronize(as_stream(stream)); e != cudaSuccess) return cuda_fail(e);
   unsigned int word = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&word, g_fp8s_error, sizeof word) != cudaSuccess ||
       cudaMemcpyToSymbol(g_fp8s_error, &zero, sizeof zero) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8S_ERR_CUDA;
+    return cuda_fail(cudaGetLastError());
   }
   if (where) *where = static_cast<int>(word);
   return word ? FP8S_ERR_DEVICE_TIMEOUT : FP8S_OK;
 }
 
 int fp8s_version(void) { return kVersion; }
+
+const char* fp8s_last_cuda_error(void) { return t_cuda_msg; }
 
 }  // extern "C"

@@ -228,8 +228,10 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 //      elements per load.
 // Small tensors use a small GPW so that the chunks still cover every SM.
 constexpr int kTgStages = 3;
-constexpr int kTgMaxChunkBytes = 8 * 16 * 256;
-constexpr int kTgSmemBytes = 1024 + kTgStages * kTgMaxChunkBytes + 64;
+// Shared memory of one CTA: sized by GPW, so that the small-GPW launches of
+// small tensors leave room for the next kernel's CTAs on the same SM
+// (programmatic dependent launch can then start them early).
+constexpr int tg_smem_bytes(int gpw) { return 1024 + kTgStages * 8 * gpw * 256 + 64; }
 
 template <int DT, int GPW>
 __global__ void __launch_bounds__(288, 2)
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(288, 2)
   constexpr int kTgChunkBytes = kTgChunkGroups * 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kTgStages * kTgMaxChunkBytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kTgStages * kTgChunkBytes);
   uint64_t* empty_bar = full_bar + kTgStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

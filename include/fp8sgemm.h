@@ -153,6 +153,13 @@ FP8S_API fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_
 FP8S_API const char* fp8s_status_string(fp8s_status status);
 
 /*
+ * fp8s_last_cuda_error -- the CUDA runtime's description of the error behind
+ * the calling host thread's most recent FP8S_ERR_CUDA (static storage, never
+ * NULL; "" before any).  Diagnostic only: no method step stands behind it.
+ */
+FP8S_API const char* fp8s_last_cuda_error(void);
+
+/*
  * fp8s_device_error -- synchronizes `stream`, then reads and clears the
  * current device's error word, which a kernel sets when one of its bounded
  * waits gives up (the kernel then exits without finishing its output).

@@ -47,6 +47,12 @@ def test_binding_covers_header(lib):
     assert set(declared_symbols()) == set(_lib.SIGNATURES)
 
 
+def test_last_cuda_error_is_text(lib):
+    """The diagnostic text is static storage, never NULL."""
+    from fp8_scaled_gemm_02_b300 import _lib
+    assert isinstance(_lib.load().fp8s_last_cuda_error(), bytes)
+
+
 def test_status_strings_and_version(lib):
     from fp8_scaled_gemm_02_b300 import _lib
     for code in range(8):
