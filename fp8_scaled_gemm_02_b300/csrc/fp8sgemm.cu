@@ -249,26 +249,112 @@ fp8s_status launch_weight_block(const void* w, int64_t N, int64_t K, uint8_t* q,
                    static_cast<int>(K / 128), static_cast<int>(nblocks), kWaitTimeoutNs);
 }
 
+// CTAs of the cooperative per-tensor kernel that fit on the device at once.
+int pt_capacity(int dev, int sms) {
+  static std::mutex mu;
+  static int cap[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  if (cap[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_per_tensor_kernel<kInF16>, kPtThreads, kPtSmemBytes) !=
+            cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cap[dev] = n * sms;
+  }
+  return cap[dev];
+}
+
+// Largest cluster (16, else 8) of the small-tensor per-tensor kernel the
+// device can schedule.
+template <int DT>
+int pt_cluster_max(int dev) {
+  static std::mutex mu;
+  static int cmax[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  if (cmax[dev] == 0) {
+    auto kern = quant_per_tensor_cluster_kernel<DT>;
+    int c = 8;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1, 1);
+      cfg.blockDim = dim3(kPtThreads, 1, 1);
+      cfg.dynamicSmemBytes = kPtSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 16;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1) c = 16;
+    }
+    cudaGetLastError();
+    cmax[dev] = c;
+  }
+  return cmax[dev];
+}
+
+// Per-tensor quantization in one launch: a tensor that fits in one cluster's
+// shared memory goes to the cluster kernel (no memset, no cooperative
+// launch); a larger one to the cooperative kernel, whose CTAs wait on each
+// other, so all of them must be resident (the launch fails otherwise).
 template <int DT>
 fp8s_status launch_per_tensor(const void* x, int64_t numel, uint8_t* q, float* scale, cudaStream_t st,
-                              const DeviceInfo& info) {
+                              const DeviceInfo& info, int dev) {
   const int64_t nvec = numel / 8;
   const int ntail = static_cast<int>(numel - nvec * 8);
   const uint16_t* tail = static_cast<const uint16_t*>(x) + nvec * 8;
+  const int64_t bytes = nvec * 16;
+  {
+    auto ckern = quant_per_tensor_cluster_kernel<DT>;
+    static bool cattr_done[kMaxDevices] = {};
+    if (fp8s_status s = ensure_smem_attr(ckern, kPtSmemBytes, cattr_done)) return s;
+    const int64_t cmax = pt_cluster_max<DT>(dev);
+    if (bytes <= cmax * kPtSliceBytes) {
+      // ~64 KB of input per CTA, at least enough CTAs to hold every slice
+      const int64_t g_res = (bytes + kPtSliceBytes - 1) / kPtSliceBytes;
+      const int64_t G = std::max(g_res, std::min(cmax, std::max<int64_t>(1, (bytes + 65535) / 65536)));
+      return launch_ex(ckern, static_cast<unsigned>(G), kPtThreads, kPtSmemBytes, st, static_cast<int>(G),
+                       static_cast<const uint4*>(x), nvec, tail, ntail, reinterpret_cast<uint2*>(q), q + nvec * 8,
+                       scale, kWaitTimeoutNs);
+    }
+  }
+  auto kern = quant_per_tensor_kernel<DT>;
+  static bool attr_done[kMaxDevices] = {};
+  if (fp8s_status s = ensure_smem_attr(kern, kPtSmemBytes, attr_done)) return s;
+  const int64_t gmax = pt_capacity(dev, info.sms);
+  // CTAs: at least 16 KB of input each (for small tensors fewer CTAs mean a
+  // cheaper exchange), enough to keep every slice in shared memory when the
+  // whole tensor fits on chip, and few enough that CTA 0's slice covers the
+  // slot words (G * (G + 1) <= 2 * nvec).
+  const int64_t g_res = (bytes + kPtSliceBytes - 1) / kPtSliceBytes;
+  int64_t G = std::min<int64_t>(gmax, std::max<int64_t>(1, (bytes + 16383) / 16384));
+  bool resident = g_res <= gmax;
+  if (resident) G = std::max(G, g_res);
+  while (G > 1 && G * (G + 1) > 2 * nvec) --G;
+  if (G < g_res) resident = false;
   unsigned int* word = reinterpret_cast<unsigned int*>(scale);
-  if (cudaMemsetAsync(word, 0, sizeof(unsigned int), st) != cudaSuccess) return launch_status(), FP8S_ERR_CUDA;
-  int64_t blocks = (nvec + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(info.sms) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  const unsigned g = static_cast<unsigned>(blocks);
-  if (fp8s_status s = launch_ex(amax_kernel<DT>, g, 256, 0, st, 1, static_cast<const uint4*>(x), nvec, tail, ntail, word))
-    return s;
-  if (fp8s_status s = launch_ex(cast_per_tensor_kernel<DT>, g, 256, 0, st, 1, static_cast<const uint4*>(x), nvec, tail,
-                                ntail, reinterpret_cast<uint2*>(q), q + nvec * 8,
-                                static_cast<const unsigned int*>(word)))
-    return s;
-  return launch_ex(finalize_scale_kernel, 1, 1, 0, st, 1, word);
+  if (const cudaError_t e = cudaMemsetAsync(word, 0, sizeof(unsigned int), st); e != cudaSuccess) return cuda_fail(e);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(G), 1, 1);
+  cfg.blockDim = dim3(kPtThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPtSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (const cudaError_t e =
+          cudaLaunchKernelEx(&cfg, kern, static_cast<const uint4*>(x), nvec, tail, ntail, reinterpret_cast<uint2*>(q),
+                             q + nvec * 8, word, resident ? 1 : 0, kWaitTimeoutNs);
+      e != cudaSuccess)
+    return cuda_fail(e);
+  return FP8S_OK;
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -457,8 +543,8 @@ fp8s_status fp8_quantize_per_tensor(const void* x, fp8s_dtype xt, int64_t numel,
   DeviceInfo info;
   if (fp8s_status s = current_device(&dev, &info)) return s;
   cudaStream_t st = as_stream(stream);
-  return xt == FP8S_F16 ? launch_per_tensor<kInF16>(x, numel, q, scale, st, info)
-                        : launch_per_tensor<kInBF16>(x, numel, q, scale, st, info);
+  return xt == FP8S_F16 ? launch_per_tensor<kInF16>(x, numel, q, scale, st, info, dev)
+                        : launch_per_tensor<kInBF16>(x, numel, q, scale, st, info, dev);
 }
 
 fp8s_status fp8_quantize_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K, uint8_t* q, float* sa,

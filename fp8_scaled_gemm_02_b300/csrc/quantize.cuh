@@ -454,64 +454,224 @@ __global__ void __launch_bounds__(kWbThreads, 1)
 }
 
 // ------------------------------------------------------------------------
-// K1: per-tensor amax.  Grid-stride over 16-byte vectors; the block maximum
-// is folded into *amax_word (the float's bit pattern; non-negative floats
-// order like unsigned integers) with one atomicMax per CTA.  *amax_word must
-// be zero beforehand.  The tail (numel % 8 elements) is read by block 0.
-template <int DT>
-__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, int64_t nvec,
-                                                   const uint16_t* __restrict__ tail, int ntail,
-                                                   unsigned int* __restrict__ amax_word) {
-  __shared__ uint32_t warp_max[8];
-  ptx::griddep_wait();
-  ptx::griddep_launch();
-  uint32_t a = 0;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    const uint4 v0 = ld_stream(x + i), v1 = ld_stream(x + i + stride);
-    const uint4 v2 = ld_stream(x + i + 2 * stride), v3 = ld_stream(x + i + 3 * stride);
-    a = max(a, max(max(amax_bits8(v0), amax_bits8(v1)), max(amax_bits8(v2), amax_bits8(v3))));
+// K1': per-tensor quantization in one cooperative launch (all CTAs resident).
+// CTA b owns the contiguous vectors [b*nvec/G, (b+1)*nvec/G).
+//  A. Amax of the slice.  When the host chose `resident` (every slice fits in
+//     kPtSliceBytes) the slice is brought into shared memory with one 1-D bulk
+//     copy and stays there, so x is read from HBM once; otherwise the slice is
+//     streamed from global memory (and streamed again in C).
+//  B. Grid exchange through the caller's own buffers, no scratch memory:
+//     CTA b stores its slice amax in the b-th 32-bit word of q, then bumps the
+//     arrival count held in *word (the caller's scale, zeroed before the
+//     launch).  When the count reaches G every CTA reads the G slot words,
+//     takes the maximum, and bumps the count again.
+//  C. Cast of the slice.  The first ceil(G/2) output vectors (they overlap
+//     the slot words) are written by CTA 0 only after the count reaches 2G,
+//     i.e. after every CTA has read the slots; CTA 0 then stores the scale
+//     over the count.
+// With G = 1 there is no exchange.  Every wait is bounded (a timeout records
+// the error and the CTA carries on, so no other CTA waits forever).
+constexpr int kPtThreads = 512;
+constexpr int kPtSliceBytes = 192 * 1024;  // input a CTA keeps in shared memory
+constexpr int kPtSmemBytes = 1024 + kPtSliceBytes + 64;
+
+template <int DT, bool kExact>
+__device__ __forceinline__ void pt_cast_range(const uint4* __restrict__ x, uint32_t slice_smem, bool resident,
+                                              int64_t v0, int64_t a, int64_t b, uint2* __restrict__ q,
+                                              const UnitScale& us) {
+  const UnitPair k(us);
+  for (int64_t i = a + threadIdx.x; i < b; i += kPtThreads) {
+    const uint4 v = resident ? lds128(slice_smem + static_cast<uint32_t>((i - v0) * 16)) : ld_stream(x + i);
+    q[i] = quant8_impl<DT, kExact>(v, us, k);
   }
-  for (; i < nvec; i += stride) a = max(a, amax_bits8(ld_stream(x + i)));
-  if (blockIdx.x == 0 && threadIdx.x < ntail) a = max(a, static_cast<uint32_t>(tail[threadIdx.x] & 0x7FFFu));
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kPtThreads, 1)
+    quant_per_tensor_kernel(const uint4* __restrict__ x, int64_t nvec, const uint16_t* __restrict__ tail, int ntail,
+                            uint2* __restrict__ q, uint8_t* __restrict__ q_tail, unsigned int* word, int resident_i,
+                            unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* slice = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(slice + kPtSliceBytes);
+  __shared__ uint32_t warp_max[kPtThreads / 32];
+  __shared__ uint32_t amax_all;
+  const bool resident = resident_i != 0;
+  const unsigned G = gridDim.x;
+  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * nvec / G;
+  const int64_t v1 = static_cast<int64_t>(blockIdx.x + 1) * nvec / G;
+  const uint32_t slice_smem = ptx::smem_u32(slice);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  ptx::griddep_wait();
+
+  // A. slice amax
+  uint32_t a = 0;
+  if (resident) {
+    const uint32_t bytes = static_cast<uint32_t>((v1 - v0) * 16);
+    if (threadIdx.x == 0) {
+      ptx::mbar_arrive_expect_tx(bar, bytes);
+      if (bytes > 0) ptx::bulk_load(slice, x + v0, bytes, bar);
+    }
+    if (!ptx::mbar_wait_bounded(bar, 0, timeout_ns)) record_quant_error();
+    for (int64_t i = threadIdx.x; i < v1 - v0; i += kPtThreads)
+      a = max(a, amax_bits8(lds128(slice_smem + static_cast<uint32_t>(i * 16))));
+  } else {
+    int64_t i = v0 + threadIdx.x;
+    for (; i + 3 * kPtThreads < v1; i += 4 * kPtThreads) {
+      const uint4 w0 = ld_stream(x + i), w1 = ld_stream(x + i + kPtThreads);
+      const uint4 w2 = ld_stream(x + i + 2 * kPtThreads), w3 = ld_stream(x + i + 3 * kPtThreads);
+      a = max(a, max(max(amax_bits8(w0), amax_bits8(w1)), max(amax_bits8(w2), amax_bits8(w3))));
+    }
+    for (; i < v1; i += kPtThreads) a = max(a, amax_bits8(ld_stream(x + i)));
+  }
+  if (blockIdx.x == 0 && threadIdx.x < static_cast<unsigned>(ntail))
+    a = max(a, static_cast<uint32_t>(tail[threadIdx.x] & 0x7FFFu));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+  __syncthreads();
+
+  // B. grid exchange of the slice maxima (magnitude patterns)
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kPtThreads / 32; ++w) a = max(a, warp_max[w]);
+    amax_all = a;
+    if (G > 1) {
+      reinterpret_cast<unsigned int*>(q)[blockIdx.x] = a;
+      __threadfence();
+      atomicAdd(word, 1u);
+      volatile unsigned int* vword = word;
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (*vword < G) {
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+          record_quant_error();
+          break;
+        }
+      }
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (G > 1) {
+    // every thread reads a share of the G slot words (one L2 round trip)
+    const unsigned int* slots = reinterpret_cast<const unsigned int*>(q);
+    uint32_t m = 0;
+    for (unsigned c = threadIdx.x; c < G; c += kPtThreads) m = max(m, __ldcg(slots + c));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    __syncthreads();  // warp_max is reused
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kPtThreads / 32; ++w) m = max(m, warp_max[w]);
+      amax_all = max(m, warp_max[0]);
+      __threadfence();
+      atomicAdd(word, 1u);  // this CTA is done with the slots
+    }
+    __syncthreads();
+  }
+  const UnitScale us(mag_to_float<DT>(amax_all));
+
+  // C. cast (CTA 0 leaves the slot-covering vectors for last)
+  const int64_t nscr = (G > 1 && blockIdx.x == 0) ? (static_cast<int64_t>(G) + 1) / 2 : 0;
+  if (us.exact_div) pt_cast_range<DT, true>(x, slice_smem, resident, v0, v0 + nscr, v1, q, us);
+  else pt_cast_range<DT, false>(x, slice_smem, resident, v0, v0 + nscr, v1, q, us);
+  if (blockIdx.x == 0) {
+    if (threadIdx.x < static_cast<unsigned>(ntail)) q_tail[threadIdx.x] = quant1<DT>(tail[threadIdx.x], us);
+    if (nscr > 0) {
+      if (threadIdx.x == 0) {
+        volatile unsigned int* vword = word;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (*vword < 2 * G) {
+          if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+            record_quant_error();
+            break;
+          }
+        }
+      }
+      __syncthreads();
+      if (us.exact_div) pt_cast_range<DT, true>(x, slice_smem, resident, v0, v0, v0 + nscr, q, us);
+      else pt_cast_range<DT, false>(x, slice_smem, resident, v0, v0, v0 + nscr, q, us);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *reinterpret_cast<float*>(word) = us.s;
+  }
+}
+
+// K1'': per-tensor quantization of a small tensor by one thread-block
+// cluster of G <= 16 CTAs (grid = one cluster; G = 1 is a plain launch).
+// The cluster is scheduled as a unit, so its CTAs may wait on each other
+// without a cooperative launch, and the exchange of the slice maxima stays
+// on chip: each CTA keeps its maximum in its own shared memory, and after a
+// cluster barrier every CTA reads all G of them through distributed shared
+// memory.  The slices (at most kPtSliceBytes each) are fetched with one bulk
+// copy and cast from shared memory.  A second cluster barrier before exit
+// keeps every CTA's shared memory alive until all peers have read it.
+template <int DT>
+__global__ void __launch_bounds__(kPtThreads, 1)
+    quant_per_tensor_cluster_kernel(const uint4* __restrict__ x, int64_t nvec, const uint16_t* __restrict__ tail,
+                                    int ntail, uint2* __restrict__ q, uint8_t* __restrict__ q_tail,
+                                    float* __restrict__ scale, unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* slice = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(slice + kPtSliceBytes);
+  __shared__ uint32_t warp_max[kPtThreads / 32];
+  __shared__ uint32_t amax_cta;  // this CTA's slice maximum, read by the peers
+  __shared__ uint32_t amax_all;
+  const unsigned G = gridDim.x;
+  const unsigned rank = blockIdx.x;
+  const int64_t v0 = static_cast<int64_t>(rank) * nvec / G;
+  const int64_t v1 = static_cast<int64_t>(rank + 1) * nvec / G;
+  const uint32_t slice_smem = ptx::smem_u32(slice);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  ptx::griddep_wait();
+  const uint32_t bytes = static_cast<uint32_t>((v1 - v0) * 16);
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    if (bytes > 0) ptx::bulk_load(slice, x + v0, bytes, bar);
+  }
+  if (!ptx::mbar_wait_bounded(bar, 0, timeout_ns)) record_quant_error();
+  uint32_t a = 0;
+  for (int64_t i = threadIdx.x; i < v1 - v0; i += kPtThreads)
+    a = max(a, amax_bits8(lds128(slice_smem + static_cast<uint32_t>(i * 16))));
+  if (rank == 0 && threadIdx.x < static_cast<unsigned>(ntail))
+    a = max(a, static_cast<uint32_t>(tail[threadIdx.x] & 0x7FFFu));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
   if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int k = 1; k < (blockDim.x >> 5); ++k) a = max(a, warp_max[k]);
-    atomicMax(amax_word, __float_as_uint(mag_to_float<DT>(a)));
+    for (int w = 1; w < kPtThreads / 32; ++w) a = max(a, warp_max[w]);
+    amax_cta = a;
   }
-}
-
-// K2: per-tensor cast with the scale derived from the finished amax.
-template <int DT>
-__global__ void __launch_bounds__(256) cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t nvec,
-                                                              const uint16_t* __restrict__ tail, int ntail,
-                                                              uint2* __restrict__ q, uint8_t* __restrict__ q_tail,
-                                                              const unsigned int* __restrict__ amax_word) {
-  ptx::griddep_wait();
-  ptx::griddep_launch();
-  const UnitScale us(__uint_as_float(*amax_word));
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + stride < nvec; i += 2 * stride) {
-    const uint4 v0 = ld_stream(x + i), v1 = ld_stream(x + i + stride);
-    q[i] = quant8<DT>(v0, us);
-    q[i + stride] = quant8<DT>(v1, us);
+  if (G > 1) {
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+    if (threadIdx.x == 0) {
+      uint32_t m = 0;
+      for (unsigned r = 0; r < G; ++r) m = max(m, ptx::ld_dsmem_u32(ptx::mapa(ptx::smem_u32(&amax_cta), r)));
+      amax_all = m;
+    }
+    ptx::cluster_arrive_relaxed();  // this CTA's reads of its peers are done (waited for before exit)
+  } else if (threadIdx.x == 0) {
+    amax_all = a;
   }
-  for (; i < nvec; i += stride) q[i] = quant8<DT>(ld_stream(x + i), us);
-  if (blockIdx.x == 0 && threadIdx.x < ntail) q_tail[threadIdx.x] = quant1<DT>(tail[threadIdx.x], us);
-}
-
-// Turns the finished amax (bits in *word) into the stored scale, in place.
-__global__ void finalize_scale_kernel(unsigned int* word) {
-  ptx::griddep_wait();
-  ptx::griddep_launch();
-  const float amax = __uint_as_float(*word);
-  const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-  *reinterpret_cast<float*>(word) = s;
+  __syncthreads();
+  const UnitScale us(mag_to_float<DT>(amax_all));
+  if (us.exact_div) pt_cast_range<DT, true>(x, slice_smem, true, v0, v0, v1, q, us);
+  else pt_cast_range<DT, false>(x, slice_smem, true, v0, v0, v1, q, us);
+  if (rank == 0) {
+    if (threadIdx.x < static_cast<unsigned>(ntail)) q_tail[threadIdx.x] = quant1<DT>(tail[threadIdx.x], us);
+    if (threadIdx.x == 0) *scale = us.s;
+  }
+  if (G > 1) ptx::cluster_wait();
 }
 
 }  // namespace fp8s

@@ -73,8 +73,15 @@ typedef enum {
  *   x      [numel] FP16/BF16 (xt), device.            numel >= 1.
  *   q      [numel] E4M3 bytes, device (output).
  *   scale  one float, device (output): s = fl32(max|x| / 448), 1 if all zero.
- * Two passes over x (an amax reduction, then the cast).  `scale` is used as
- * the reduction's accumulator while the call runs; its final value is s.
+ * One kernel launch.  Up to 3 MB of input: one thread-block cluster whose
+ * CTAs exchange their slice maxima through distributed shared memory.
+ * Larger: one cooperative launch (its CTAs wait on each other, so all of them
+ * are resident; the launch fails with FP8S_ERR_CUDA if the device cannot
+ * hold them) whose CTAs exchange their slice maxima through `scale` (an
+ * arrival count while the call runs; its final value is s) and the first
+ * 4*G bytes of q (G = CTAs).  Up to ~29 MB of input (148 CTAs x 192 KB of
+ * shared memory) is read from HBM once, a larger x twice.  Neither q nor
+ * scale may be read or written by anything else while the call runs.
  */
 FP8S_API fp8s_status fp8_quantize_per_tensor(const void* x, fp8s_dtype xt, int64_t numel,
                                     uint8_t* q, float* scale, fp8s_stream_t stream);
