@@ -63,6 +63,35 @@ def test_per_tensor_parity(dtype, numel):
     check_per_tensor(bits, dtype)
 
 
+# The per-tensor quantizer switches paths by input size: one cluster of up
+# to 16 CTAs (each slice <= 192 KB of shared memory) up to 16 * 192 KB of
+# input, then a cooperative launch that keeps slices in shared memory up to
+# 148 * 192 KB, and streams them beyond that.  These sizes sit on both sides
+# of each switch, with and without a tail of numel % 8 elements.
+SLICE_ELEMS = 192 * 1024 // 2
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("numel", [16 * SLICE_ELEMS, 16 * SLICE_ELEMS + 8, 16 * SLICE_ELEMS + 3,
+                                   148 * SLICE_ELEMS - 8, 148 * SLICE_ELEMS + 8, 148 * SLICE_ELEMS + 5,
+                                   3 * SLICE_ELEMS + 1])
+def test_per_tensor_path_boundaries(dtype, numel):
+    bits = synth.random_bits((numel,), dtype, seed=34, tensor_id=numel, std=3.0)
+    check_per_tensor(bits, dtype)
+
+
+def test_per_tensor_single_outlier_in_last_slice():
+    """The maximum sits in the last CTA's slice (and in the tail): every
+    other CTA must take it from the exchange."""
+    for numel in (1000003, 16 * SLICE_ELEMS + 7, 148 * SLICE_ELEMS + 7):
+        bits = synth.random_bits((numel,), "bf16", seed=35, tensor_id=numel, std=1.0)
+        bits[-1] = 0x4700  # bf16 32768.0, far above the rest
+        check_per_tensor(bits, "bf16")
+        bits[-1] = 0x3F80
+        bits[-9] = 0xC700  # -32768.0 in the last full vector
+        check_per_tensor(bits, "bf16")
+
+
 def test_zero_and_negative_zero_units():
     z = np.zeros((3, 384), np.uint16)
     z[1, 128:256] = 0x8000
