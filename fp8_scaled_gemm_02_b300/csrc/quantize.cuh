@@ -13,25 +13,24 @@
 //    finite FP16/BF16 magnitudes order exactly like unsigned integers, so a
 //    packed 16-bit unsigned max (__vmaxu2) is an exact max.
 //  * the E4M3 byte of fl32(x / s) is obtained without a per-element divide.
-//    With y the correctly rounded reciprocal of s (computed once per unit),
-//    q0 = RN(x*y) is refined once by the exact remainder r = x - s*q0 (an
-//    FMA) to q = RN(q0 + r*y) (Markstein, "IA-64 and Elementary Functions",
-//    division by reciprocal refinement), two elements at a time with the
-//    packed .f32x2 FMA.  q can still differ from fl32(x/s) in the last
-//    place, but never across an E4M3 rounding boundary: for every pair of
-//    FP16 or BF16 magnitudes |x| <= amax (all ~5 * 10^8 of each) the byte
-//    cvt(q) equals cvt(fl32(x/s)), which an exhaustive test checks through
-//    the token-group entry point against the oracle.  (q0 alone is not
+//    Once per unit: y = RN(1/s), and ylo = RN(r*y) with the residual
+//    r = 1 - s*y (exact through an FMA), so that y + ylo is 1/s to about
+//    2^-47 (a double-word reciprocal).  Per element: q = RN(x*y + RN(x*ylo))
+//    (a multiply and an FMA, two elements at a time with the packed .f32x2
+//    instructions).  q can differ from fl32(x/s) in the last place, but
+//    never across an E4M3 rounding boundary: for every pair of FP16 or BF16
+//    magnitudes |x| <= amax (about 5 * 10^8 of each) the byte cvt(q) equals
+//    cvt(fl32(x/s)), which an exhaustive test checks through the
+//    token-group entry point against the oracle.  (RN(x*y) alone is not
 //    enough: it differs at about 5 in 10^5 pairs, where x/s lies on or next
 //    to an E4M3 midpoint.)  Elements never exceed their unit's amax, so
 //    these pairs are every input the quantizers can see.
-//    The only value this sequence gets wrong in sign is an input of -0 (the
-//    sum of the two zero terms rounds to +0), and the E4M3 code of -0/s is
-//    0x80: so the input's sign bit is OR-ed into every code, which changes
-//    nothing else (a negative non-zero quotient already has its sign bit,
-//    including one that rounds to zero).  Units whose scale is tiny
-//    (s < 2^-90, possible only for BF16 inputs below about 2^-81) use the
-//    IEEE divide __fdiv_rn.
+//    The sign of a zero quotient can come out wrong (x = -0 with ylo > 0
+//    gives -0 + +0 = +0), and the E4M3 code of -0/s is 0x80: so the input's
+//    sign bit is OR-ed into every code, which changes nothing else (a
+//    negative non-zero quotient already has its sign bit, including one
+//    that rounds to zero).  Units whose scale is tiny (s < 2^-90, possible
+//    only for BF16 inputs below about 2^-81) use the IEEE divide __fdiv_rn.
 //  * the E4M3 rounding is the hardware cvt.rn.satfinite.e4m3x2.f32.
 #pragma once
 
@@ -80,34 +79,31 @@ __device__ __forceinline__ uint32_t amax_bits8(const uint4& v) {
   return max(m & 0xFFFFu, m >> 16);
 }
 
-// Exact fl32(x / s) for one quantization unit (see the file comment).
+// The quotient x / s of one quantization unit, to E4M3 precision (see the
+// file comment).
 struct UnitScale {
   float s;     // dequant factor written to memory
   float y;     // RN(1/s)
+  float ylo;   // RN((1 - s*y) * y): 1/s ~ y + ylo to about 2^-47
   bool exact_div;
 
-  __device__ __forceinline__ UnitScale() : s(1.0f), y(1.0f), exact_div(false) {}
-  __device__ __forceinline__ UnitScale(float s_, float y_, bool e_) : s(s_), y(y_), exact_div(e_) {}
+  __device__ __forceinline__ UnitScale() : s(1.0f), y(1.0f), ylo(0.0f), exact_div(false) {}
+  __device__ __forceinline__ UnitScale(float s_, float y_, bool e_) : s(s_), y(y_), exact_div(e_) {
+    ylo = __fmul_rn(__fmaf_rn(-s, y, 1.0f), y);
+  }
   __device__ __forceinline__ explicit UnitScale(float amax) {
     s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
     y = __frcp_rn(s);
+    ylo = __fmul_rn(__fmaf_rn(-s, y, 1.0f), y);  // the residual 1 - s*y is exact (FMA)
     exact_div = !(s >= 0x1p-90f);
   }
 
-  // q0 = RN(x*y) and one Markstein step, q = RN(q0 + r*y) with the exact
-  // remainder r = x - s*q0; valid when !exact_div.  For every FP16 and BF16
-  // pair |x| <= amax this q rounds to the same E4M3 byte as the IEEE
-  // quotient fl32(x/s) (checked exhaustively over all such pairs; with q0
-  // alone about 5 in 10^5 pairs differ, at quotients on or next to an E4M3
-  // rounding midpoint).  The remainder is formed negated, r' = s*q0 - x, and
-  // the step is q0 - r'*y: for x != 0 this is the same rounding of the same
-  // exact value, and for x = -0 (or a quotient that underflows to zero) the
-  // sum of two like-signed zeros keeps the sign of x.
-  __device__ __forceinline__ float div_fast(float x) const {
-    const float q = __fmul_rn(x, y);
-    const float r = __fmaf_rn(s, q, -x);
-    return __fmaf_rn(-r, y, q);
-  }
+  // q = RN(x*y + RN(x*ylo)): x times the double-word reciprocal y + ylo,
+  // valid when !exact_div.  For every FP16 and BF16 pair |x| <= amax this q
+  // rounds to the same E4M3 byte as the IEEE quotient fl32(x/s) (checked
+  // exhaustively over all such pairs; with RN(x*y) alone about 5 in 10^5
+  // pairs differ, at quotients on or next to an E4M3 rounding midpoint).
+  __device__ __forceinline__ float div_fast(float x) const { return __fmaf_rn(x, y, __fmul_rn(x, ylo)); }
 
   __device__ __forceinline__ float div_exact(float x) const { return __fdiv_rn(x, s); }
 };
@@ -123,11 +119,11 @@ __device__ __forceinline__ uint64_t unpack2_f2(uint32_t w) {
   }
 }
 
-// The unit's constants for the packed refinement: {-s, -s} and {y, y}.
+// The unit's reciprocal words as FP32 pairs: {y, y} and {ylo, ylo}.
 struct UnitPair {
-  uint64_t nss, yy;
+  uint64_t yy, ll;
   __device__ __forceinline__ explicit UnitPair(const UnitScale& us)
-      : nss(ptx::f2_pack(-us.s, -us.s)), yy(ptx::f2_pack(us.y, us.y)) {}
+      : yy(ptx::f2_pack(us.y, us.y)), ll(ptx::f2_pack(us.ylo, us.ylo)) {}
 };
 
 // Two packed 16-bit inputs -> two E4M3 bytes (low input in the low byte),
@@ -135,9 +131,7 @@ struct UnitPair {
 template <int DT>
 __device__ __forceinline__ uint32_t quant2_fast(uint32_t w, const UnitPair& k) {
   const uint64_t x = unpack2_f2<DT>(w);
-  uint64_t q = ptx::f2_mul(x, k.yy);
-  const uint64_t r = ptx::f2_fma(k.nss, q, x);  // x - s*q, exact
-  q = ptx::f2_fma(r, k.yy, q);                   // one Markstein step (see UnitScale::div_fast)
+  const uint64_t q = ptx::f2_fma(x, k.yy, ptx::f2_mul(x, k.ll));  // as UnitScale::div_fast
   float lo, hi;
   ptx::f2_unpack(q, lo, hi);
   return ptx::cvt_e4m3x2(hi, lo);
