@@ -469,6 +469,21 @@ constexpr int kPtThreads = 512;
 constexpr int kPtSliceBytes = 192 * 1024;  // input a CTA keeps in shared memory
 constexpr int kPtSmemBytes = 1024 + kPtSliceBytes + 64;
 
+// Brings a slice (bytes a multiple of 16) into shared memory as 16 KB bulk
+// copies issued by the lanes of warp 0, all completing on `bar`: many copies
+// in flight keep an SM's ingest rate up where one large copy would not.
+__device__ __forceinline__ void pt_load_slice(uint8_t* dst, const uint4* src, uint32_t bytes, uint64_t* bar) {
+  constexpr uint32_t kChunk = 16 * 1024;
+  if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar, bytes);
+  __syncwarp();
+  if (threadIdx.x < 32) {
+    for (uint32_t off = threadIdx.x * kChunk; off < bytes; off += 32 * kChunk) {
+      const uint32_t n = bytes - off < kChunk ? bytes - off : kChunk;
+      ptx::bulk_load(dst + off, reinterpret_cast<const uint8_t*>(src) + off, n, bar);
+    }
+  }
+}
+
 template <int DT, bool kExact>
 __device__ __forceinline__ void pt_cast_range(const uint4* __restrict__ x, uint32_t slice_smem, bool resident,
                                               int64_t v0, int64_t a, int64_t b, uint2* __restrict__ q,
@@ -505,11 +520,7 @@ __global__ void __launch_bounds__(kPtThreads, 1)
   // A. slice amax
   uint32_t a = 0;
   if (resident) {
-    const uint32_t bytes = static_cast<uint32_t>((v1 - v0) * 16);
-    if (threadIdx.x == 0) {
-      ptx::mbar_arrive_expect_tx(bar, bytes);
-      if (bytes > 0) ptx::bulk_load(slice, x + v0, bytes, bar);
-    }
+    pt_load_slice(slice, x + v0, static_cast<uint32_t>((v1 - v0) * 16), bar);
     if (!ptx::mbar_wait_bounded(bar, 0, timeout_ns)) record_quant_error();
     for (int64_t i = threadIdx.x; i < v1 - v0; i += kPtThreads)
       a = max(a, amax_bits8(lds128(slice_smem + static_cast<uint32_t>(i * 16))));
@@ -626,11 +637,7 @@ __global__ void __launch_bounds__(kPtThreads, 1)
   }
   __syncthreads();
   ptx::griddep_wait();
-  const uint32_t bytes = static_cast<uint32_t>((v1 - v0) * 16);
-  if (threadIdx.x == 0) {
-    ptx::mbar_arrive_expect_tx(bar, bytes);
-    if (bytes > 0) ptx::bulk_load(slice, x + v0, bytes, bar);
-  }
+  pt_load_slice(slice, x + v0, static_cast<uint32_t>((v1 - v0) * 16), bar);
   if (!ptx::mbar_wait_bounded(bar, 0, timeout_ns)) record_quant_error();
   uint32_t a = 0;
   for (int64_t i = threadIdx.x; i < v1 - v0; i += kPtThreads)
