@@ -5,6 +5,9 @@ One step = one pass of the whole path over one batch of synthetic input, for
 every linear of the workload and every scaling mode it uses:
   block mode:      token-group quantize of A, block quantize of W, GEMM
   per-tensor mode: per-tensor quantize of A and of W, GEMM
+The two quantizations of a linear are independent: A's runs on a forked
+stream while W's runs on the main one, and the GEMM follows both (the
+fork and join are events inside the captured graph).
 `value` is the step's GEMM FLOPs divided by the step time (TFLOP/s), inputs
 resident in HBM.  L2 is defeated by rotating over enough copies of the
 inputs that consecutive uses of one copy are more than 2x the L2 size apart.
@@ -308,6 +311,25 @@ def run_ours(args):
                                                            mode="per_tensor", c=b["c"]))
         return calls
 
+    side = torch.cuda.Stream(device=dev)
+
+    def run_step(r, main):
+        """One step on stream `main`: per linear, the activation is quantized
+        on a forked stream while the weight is quantized on `main` (the two
+        are independent), then the GEMM runs on `main` after both."""
+        calls = kernel_calls(r)
+        for i in range(0, len(calls), 3):
+            ev_fork = torch.cuda.Event()
+            ev_fork.record(main)
+            side.wait_event(ev_fork)
+            with torch.cuda.stream(side):
+                calls[i]()
+            calls[i + 1]()
+            ev_join = torch.cuda.Event()
+            ev_join.record(side)
+            main.wait_event(ev_join)
+            calls[i + 2]()
+
     kinfo = [k for _, _, ks in plan for k in ks]
     launches_per_kernel = [1 for _ in kinfo]
 
@@ -340,13 +362,14 @@ def run_ours(args):
 
     def capture(steps, only=None):
         """Graph of `steps` consecutive steps (rotating input sets); with
-        `only` = j, just kernel j of each step."""
+        `only` = j, just kernel j of each step (back to back on one stream)."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(steps):
-                for j, c in enumerate(kernel_calls(i % R)):
-                    if only is None or only == j:
-                        c()
+                if only is None:
+                    run_step(i % R, stream)
+                else:
+                    kernel_calls(i % R)[only]()
         return g
 
     K, W = args.steps, args.warmup
@@ -428,8 +451,7 @@ def run_ours(args):
                 s["a"][k].copy_(t, non_blocking=True)
             for k, t in pin_w.items():
                 s["w"][k].copy_(t, non_blocking=True)
-            for c in kernel_calls(r):
-                c()
+            run_step(r, stream)
             for b, hc in zip(s["lin"], pin_c):
                 hc.copy_(b["c"], non_blocking=True)
 
