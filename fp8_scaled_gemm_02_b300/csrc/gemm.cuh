@@ -244,6 +244,66 @@ __device__ __forceinline__ void release_tmem(uint64_t* bar) {
   else ptx::mbar_arrive(bar);
 }
 
+// Sums this CTA's R = 128/S rows over the S partials in rank order (its own
+// in `send`, peer q's in receive slot q < rank ? q : q - 1), rounds and
+// stores them.  S is a template parameter so that the S loads of an output
+// vector are issued together; each thread takes two 4-column vectors per
+// iteration.
+template <int BN, int OUT, int S>
+__device__ __forceinline__ void reduce_rows(const float* send, const float* recv, uint32_t rank, int tid, int nthreads,
+                                            int tm, int tn, const GemmParams& p) {
+  constexpr int kPitch = BN + 4;
+  constexpr int kVecPerRow = BN / 4;
+  constexpr int R = kBM / S;
+  constexpr int kTotal = R * kVecPerRow;
+  uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
+  const bool vec_ok = (p.N % 4) == 0;
+  const float* src[S];
+#pragma unroll
+  for (int q = 0; q < S; ++q)
+    src[q] = q == static_cast<int>(rank) ? send + static_cast<int>(rank) * R * kPitch
+                                         : recv + (q < static_cast<int>(rank) ? q : q - 1) * R * kPitch;
+  for (int v0 = tid; v0 < kTotal; v0 += 2 * nthreads) {
+    float4 t[2][S];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int v = v0 + u * nthreads;
+      const int off = (v / kVecPerRow) * kPitch + (v % kVecPerRow) * 4;
+#pragma unroll
+      for (int q = 0; q < S; ++q)
+        t[u][q] = v < kTotal ? *reinterpret_cast<const float4*>(src[q] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int v = v0 + u * nthreads;
+      if (v >= kTotal) continue;
+      float4 acc = t[u][0];
+#pragma unroll
+      for (int q = 1; q < S; ++q) {
+        acc.x += t[u][q].x;
+        acc.y += t[u][q].y;
+        acc.z += t[u][q].z;
+        acc.w += t[u][q].w;
+      }
+      const int row = tm * kBM + static_cast<int>(rank) * R + v / kVecPerRow;
+      const int n = tn * BN + (v % kVecPerRow) * 4;
+      if (row >= p.M) continue;
+      uint16_t* crow = C + static_cast<int64_t>(row) * p.N;
+      if (vec_ok && n + 4 <= p.N) {
+        uint2 pk;
+        pk.x = pack_out<OUT>(acc.x, acc.y);
+        pk.y = pack_out<OUT>(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(crow + n) = pk;
+      } else {
+        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (n + j < p.N) crow[n + j] = one_out<OUT>(a4[j]);
+      }
+    }
+  }
+}
+
 // Split-K exchange, pushed through the cluster's shared memory.  Rank r of
 // S owns output rows [r*R, (r+1)*R), R = 128/S.  Once every epilogue warp of
 // this CTA has written its part of the partial into `send` (signalled on the
@@ -260,7 +320,6 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
                                                     const float* recv, uint32_t rank, uint32_t S, int tid,
                                                     int nthreads, int tm, int tn, const GemmParams& p) {
   constexpr int kPitch = BN + 4;
-  constexpr int kVecPerRow = BN / 4;
   const int R = kBM / static_cast<int>(S);
   const uint32_t slice_bytes = static_cast<uint32_t>(R * kPitch * 4);
   const int lane = tid & 31;
@@ -288,41 +347,10 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
     record_error(kErrEpilogue);
     return false;
   }
-  uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
-  const bool vec_ok = (p.N % 4) == 0;
-  const int total = R * kVecPerRow;
-  for (int v = tid; v < total; v += nthreads) {
-    const int rl = v / kVecPerRow;           // row within the slice
-    const int c4 = (v % kVecPerRow) * 4;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (uint32_t q = 0; q < S; ++q) {
-      const float* src = q == rank ? send + (static_cast<int>(rank) * R + rl) * kPitch
-                                   : recv + ((q < rank ? q : q - 1) * R + rl) * kPitch;
-      const float4 t = *reinterpret_cast<const float4*>(src + c4);
-      if (q == 0) {
-        acc = t;
-      } else {
-        acc.x += t.x;
-        acc.y += t.y;
-        acc.z += t.z;
-        acc.w += t.w;
-      }
-    }
-    const int row = tm * kBM + static_cast<int>(rank) * R + rl;
-    const int n = tn * BN + c4;
-    if (row >= p.M) continue;
-    uint16_t* crow = C + static_cast<int64_t>(row) * p.N;
-    if (vec_ok && n + 4 <= p.N) {
-      uint2 pk;
-      pk.x = pack_out<OUT>(acc.x, acc.y);
-      pk.y = pack_out<OUT>(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(crow + n) = pk;
-    } else {
-      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (n + j < p.N) crow[n + j] = one_out<OUT>(a4[j]);
-    }
+  switch (S) {
+    case 2: reduce_rows<BN, OUT, 2>(send, recv, rank, tid, nthreads, tm, tn, p); break;
+    case 4: reduce_rows<BN, OUT, 4>(send, recv, rank, tid, nthreads, tm, tn, p); break;
+    default: reduce_rows<BN, OUT, 8>(send, recv, rank, tid, nthreads, tm, tn, p); break;
   }
   return true;
 }
