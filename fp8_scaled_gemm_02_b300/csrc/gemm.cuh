@@ -630,6 +630,50 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
         const float* sa_col = p.sa + (row < p.M ? row : 0);
         const float* sb_row = p.sb + static_cast<int64_t>(nb) * p.num_kb;
         const int rot = kb_rotation(tm, tn, nkb);
+        if constexpr (Cfg::kSeqChunks) {
+          // One K block at a time, kSeqLoadCols columns per wait: the
+          // accumulators + the staged columns fit the register budget.  The
+          // K block index walks the tile's rotated order incrementally and
+          // the next block's scales are loaded one block ahead.
+          constexpr int LC = Cfg::kSeqLoadCols;
+          const int64_t sa_step = p.M;
+          const int kb_stop = kb_begin + nkb;
+          const uint32_t taddr0 = tmem_base + lane_off + static_cast<uint32_t>(wg * CPT);
+          int kb = kb_begin + rot;
+          float sa_c = __ldg(sa_col + kb * sa_step), sb_c = __ldg(sb_row + kb);
+          for (int i = 0; i < nkb; ++i) {
+            const float sc = sa_c * sb_c;
+            const int kn = kb + 1 == kb_stop ? kb_begin : kb + 1;
+            if (i + 1 < nkb) {
+              sa_c = __ldg(sa_col + kn * sa_step);
+              sb_c = __ldg(sb_row + kn);
+            }
+            kb = kn;
+            const uint32_t buf = unit % NBUF;
+            if (!ptx::mbar_wait_bounded(&tfull_bar[buf], (unit / NBUF) & 1, p.timeout_ns)) {
+              record_error(kErrEpilogue);
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t taddr = taddr0 + buf * BN;
+#pragma unroll
+            for (int c0 = 0; c0 < CPT; c0 += LC) {
+              uint32_t part[LC];
+#pragma unroll
+              for (int c = 0; c < LC; c += CW) tmem_load_nowait<CW>(taddr + c0 + c, &part[c]);
+              ptx::tmem_ld_wait();
+              if (c0 + LC == CPT) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_tmem<PAIR>(&tempty_bar[buf]);
+              }
+#pragma unroll
+              for (int j = 0; j < LC; j += 2) promote2(&acc[c0 + j], part[j], part[j + 1], sc);
+            }
+            unit += 1;
+          }
+        } else {
         // global K block of the i-th K block issued for this tile
         auto kb_at = [&](int i) { return kb_begin + (i + rot < nkb ? i + rot : i + rot - nkb); };
         float sa_n[KBT], sb_n[KBT];
@@ -657,27 +701,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
           }
           if (!ok) break;
           ptx::tc_fence_after();
-          if constexpr (Cfg::kSeqChunks) {
-            // One K block at a time, kSeqLoadCols columns per wait: the
-            // accumulators + the staged columns fit the register budget.
-            constexpr int LC = Cfg::kSeqLoadCols;
-            const uint32_t col0 = (unit % NBUF) * BN + wg * CPT;
-#pragma unroll
-            for (int c0 = 0; c0 < CPT; c0 += LC) {
-              uint32_t part[LC];
-#pragma unroll
-              for (int c = 0; c < LC; c += CW) tmem_load_nowait<CW>(tmem_base + lane_off + col0 + c0 + c, &part[c]);
-              ptx::tmem_ld_wait();
-              if (c0 + LC == CPT) {
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) release_tmem<PAIR>(&tempty_bar[unit % NBUF]);
-              }
-#pragma unroll
-              for (int j = 0; j < LC; j += 2) promote2(&acc[c0 + j], part[j], part[j + 1], sc[0]);
-            }
-            unit += 1;
-          } else {
+          {
             uint32_t part[KBT][CPT];
 #pragma unroll
             for (int j = 0; j < KBT; ++j) {
@@ -701,6 +725,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
                 for (int c = 0; c < CPT; c += 2) promote2(&acc[c], part[j][c], part[j][c + 1], sc[j]);
               }
           }
+        }
         }
         if (!ok) break;
         if constexpr (SPLIT) {
