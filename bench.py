@@ -71,6 +71,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(x, world, device):
+    """The largest x over all ranks, returned on every rank (the slowest
+    rank's time is the job's time); x itself when there is one rank."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, flops_per_step, step_ms):
+    """Whole-job TFLOP/s of `world` replicas that each ran one step of
+    flops_per_step in step_ms (already the maximum over ranks)."""
+    return world * flops_per_step / (step_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ algorithmic work
 def kernel_plan(wl):
     """[(linear, mode, [(kernel name, bound, bytes, flops)])] of one step."""
@@ -387,12 +405,8 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def rank_max(x):
+        return max_over_ranks(x, world, dev)
 
     sampler = ClockSampler(local)
     if sampler.ok:
@@ -419,7 +433,7 @@ def run_ours(args):
         ev1.record(stream)
         barrier()
         t1 = time.perf_counter()
-        step_ms = max_over_ranks(ev0.elapsed_time(ev1)) / K
+        step_ms = rank_max(ev0.elapsed_time(ev1)) / K
 
         # ---- kernel region: each kernel alone, Kk back-to-back launches
         kern_ms = []
@@ -431,7 +445,7 @@ def run_ours(args):
             g_kern[j].replay()
             eb.record(stream)
             barrier()
-            kern_ms.append(max_over_ranks(ea.elapsed_time(eb)) / Kk)
+            kern_ms.append(rank_max(ea.elapsed_time(eb)) / Kk)
         kregion_step_ms = sum(kern_ms)
     sampler.stop_flag.set()
     assert F.fp8s_device_error() == 0, "a kernel's bounded wait expired during the benchmark"
@@ -471,9 +485,9 @@ def run_ours(args):
                 e2e_step(i % R)
             eb.record(stream)
             barrier()
-            e2e_ms = max_over_ranks(ea.elapsed_time(eb)) / ke
+            e2e_ms = rank_max(ea.elapsed_time(eb)) / ke
         flops_step = sum(k[3] for k in kinfo)
-        e2e = {"value": round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+        e2e = {"value": round(replica_throughput(world, flops_step, e2e_ms), 4), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": round(e2e_ms, 5)}
 
     # ---- numbers
@@ -519,7 +533,7 @@ def run_ours(args):
     roof["per_launch"] = {"bytes": d["bytes"] // nl, "flops": d["flops"] // nl, "ms": round(d["ms"] / nl, 6)}
 
     flops_step = sum(k[3] for k in kinfo)
-    value = world * flops_step / (step_ms * 1e-3) / 1e12
+    value = replica_throughput(world, flops_step, step_ms)
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(step_ms, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

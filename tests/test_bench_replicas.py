@@ -1,0 +1,67 @@
+"""The N > 1 bookkeeping of bench.py, on two gloo ranks on CPU.
+
+Multi-GPU here is replicas only: every rank runs its own copy of the
+workload, with no collective on the data path.  What N > 1 changes is the
+reporting: the job's step time is the slowest rank's (a max-reduction after
+a barrier), the throughput counts the work of every rank, and the reference
+arm runs on rank 0 alone."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    step_ms = 1.5 * (rank + 1)  # rank r took 1.5 * (r + 1) ms per step
+    slowest = bench.max_over_ranks(step_ms, world, "cpu")
+    value = bench.replica_throughput(world, 2e12, slowest)  # 2 TFLOP per step per replica
+    dist.barrier()
+    dist.destroy_process_group()
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump({"slowest": slowest, "value": value}, f)
+
+
+def test_two_gloo_ranks_take_the_slowest_rank_and_count_both(tmp_path):
+    import torch.multiprocessing as mp
+    mp.start_processes(_rank_main, args=(2, _free_port(), str(tmp_path)), nprocs=2, start_method="spawn", join=True)
+    r = [json.load(open(tmp_path / f"r{k}.json")) for k in range(2)]
+    assert r[0]["slowest"] == r[1]["slowest"] == 3.0
+    assert r[0]["value"] == pytest.approx(2 * 2e12 / 3.0e-3 / 1e12)
+    assert r[1]["value"] == r[0]["value"]
+
+
+def test_one_rank_reports_its_own_time():
+    import bench
+    assert bench.max_over_ranks(2.5, 1, "cpu") == 2.5
+    assert bench.replica_throughput(1, 1e12, 1.0) == pytest.approx(1000.0)
+
+
+def test_reference_arm_prints_on_rank_zero_only(monkeypatch, capsys):
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class Args:
+        workload = bench.DEFAULT_WORKLOAD
+        steps = 1
+        warmup = 0
+
+    bench.run_reference(Args())
+    assert capsys.readouterr().out == ""
