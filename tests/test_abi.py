@@ -137,6 +137,8 @@ def test_gemm_plan_matches_measured_choices(lib):
     assert plan(lib, 4096, 22016, 4096, BLOCK) == (256, 1, 0)    # large: widest single-CTA tile
     assert plan(lib, 16384, 8192, 8192, PT) == (256, 1, 1)       # large per-tensor: CTA pairs
     assert plan(lib, 512, 2048, 2048, PT)[2] == 0                # no pair when it cannot pay for its start-up
+    assert plan(lib, 512, 11264, 2048, PT) == (192, 1, 0)      # M = 512: single-CTA 17.7 us vs paired 19.8 us
+    assert plan(lib, 4096, 12288, 4096, PT)[2] == 1             # from M = 1024 up pairs pay off
     bn, sp, pr = plan(lib, 64, 64, 128, PT)
     assert sp == 1 and pr == 0
 
