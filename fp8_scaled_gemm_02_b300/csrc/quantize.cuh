@@ -195,6 +195,22 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// 16-byte load that does not allocate in L1 and asks L2 to keep the line
+// (evict-last policy `pol`, from createpolicy): for data read again soon.
+__device__ __forceinline__ uint4 ld_keep_l2(const uint4* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Streaming 16-byte load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -499,7 +515,18 @@ __device__ __forceinline__ void pt_cast_range(const uint4* __restrict__ x, uint3
                                               int64_t v0, int64_t a, int64_t b, uint2* __restrict__ q,
                                               const UnitScale& us) {
   const UnitPair k(us);
-  for (int64_t i = a + threadIdx.x; i < b; i += kPtThreads) {
+  int64_t i = a + threadIdx.x;
+  if (!resident) {
+    // from global memory: four loads in flight per thread before any cast
+    for (; i + 3 * kPtThreads < b; i += 4 * kPtThreads) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = ld_stream(x + i + u * kPtThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[i + u * kPtThreads] = quant8_impl<DT, kExact>(v[u], us, k);
+    }
+  }
+  for (; i < b; i += kPtThreads) {
     const uint4 v = resident ? lds128(slice_smem + static_cast<uint32_t>((i - v0) * 16)) : ld_stream(x + i);
     q[i] = quant8_impl<DT, kExact>(v, us, k);
   }
@@ -535,13 +562,17 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     for (int64_t i = threadIdx.x; i < v1 - v0; i += kPtThreads)
       a = max(a, amax_bits8(lds128(slice_smem + static_cast<uint32_t>(i * 16))));
   } else {
+    // first of two passes over x: ask L2 to keep the lines for the cast pass
+    const uint64_t pol = l2_evict_last_policy();
     int64_t i = v0 + threadIdx.x;
-    for (; i + 3 * kPtThreads < v1; i += 4 * kPtThreads) {
-      const uint4 w0 = ld_stream(x + i), w1 = ld_stream(x + i + kPtThreads);
-      const uint4 w2 = ld_stream(x + i + 2 * kPtThreads), w3 = ld_stream(x + i + 3 * kPtThreads);
-      a = max(a, max(max(amax_bits8(w0), amax_bits8(w1)), max(amax_bits8(w2), amax_bits8(w3))));
+    for (; i + 7 * kPtThreads < v1; i += 8 * kPtThreads) {  // eight loads in flight per thread
+      uint4 w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w[u] = ld_keep_l2(x + i + u * kPtThreads, pol);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a = max(a, amax_bits8(w[u]));
     }
-    for (; i < v1; i += kPtThreads) a = max(a, amax_bits8(ld_stream(x + i)));
+    for (; i < v1; i += kPtThreads) a = max(a, amax_bits8(ld_keep_l2(x + i, pol)));
   }
   if (blockIdx.x == 0 && threadIdx.x < static_cast<unsigned>(ntail))
     a = max(a, static_cast<uint32_t>(tail[threadIdx.x] & 0x7FFFu));
