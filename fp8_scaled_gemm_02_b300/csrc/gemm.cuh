@@ -336,8 +336,10 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
     // before this; the phase cannot complete until this arrival.
     ptx::mbar_arrive_expect_tx(recv_bar, (S - 1) * slice_bytes);
     const uint32_t send0 = ptx::smem_u32(send), recv0 = ptx::smem_u32(recv), rbar = ptx::smem_u32(recv_bar);
-    for (uint32_t q = 0; q < S; ++q) {
-      if (q == rank) continue;
+    // peers in the order rank+1, rank+2, ...: the S CTAs start on S
+    // different destinations instead of all sending to rank 0 first
+    for (uint32_t i = 1; i < S; ++i) {
+      const uint32_t q = (rank + i) % S;
       const uint32_t slot = rank < q ? rank : rank - 1;  // this CTA's slot in q's receive buffer
       ptx::bulk_copy_to_peer(ptx::mapa(recv0 + slot * slice_bytes, q), send0 + q * slice_bytes, slice_bytes,
                              ptx::mapa(rbar, q));
