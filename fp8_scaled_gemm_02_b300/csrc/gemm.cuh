@@ -341,8 +341,12 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
     for (uint32_t i = 1; i < S; ++i) {
       const uint32_t q = (rank + i) % S;
       const uint32_t slot = rank < q ? rank : rank - 1;  // this CTA's slot in q's receive buffer
-      ptx::bulk_copy_to_peer(ptx::mapa(recv0 + slot * slice_bytes, q), send0 + q * slice_bytes, slice_bytes,
+      // two copies per slice (both 16-byte multiples): more requests in flight
+      const uint32_t h = (slice_bytes / 2) & ~15u;
+      ptx::bulk_copy_to_peer(ptx::mapa(recv0 + slot * slice_bytes, q), send0 + q * slice_bytes, h,
                              ptx::mapa(rbar, q));
+      ptx::bulk_copy_to_peer(ptx::mapa(recv0 + slot * slice_bytes + h, q), send0 + q * slice_bytes + h,
+                             slice_bytes - h, ptx::mapa(rbar, q));
     }
   }
   if (!ptx::mbar_wait_bounded(recv_bar, 0, p.timeout_ns)) {
