@@ -55,6 +55,8 @@ def _load():
             "oracle_to_float_array": (None, [P, I, I64, P]),
             "oracle_quantize_with_scale": (None, [P, I, I64, F, P]),
             "oracle_quantize_scales_grid": (None, [P, I, I64, P, I64, P]),
+            "oracle_scale_from_history": (F, [P, I64, I]),
+            "oracle_amax": (F, [P, I, I64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -165,6 +167,20 @@ def quantize_with_scale(x, dtype, s) -> np.ndarray:
     q = np.empty(x.shape, np.uint8)
     _load().oracle_quantize_with_scale(_ptr(x), _dt(dtype), x.size, float(np.float32(s)), _ptr(q))
     return q
+
+
+def amax(x, dtype) -> np.float32:
+    """max|x| over all elements, as FP32 (exact)."""
+    x = _u16(x)
+    return np.float32(_load().oracle_amax(_ptr(x), _dt(dtype), x.size))
+
+
+def scale_from_history(history, margin=0) -> np.float32:
+    """Delayed scaling: fl32(max(history) / 448) * 2**margin (1 * 2**margin
+    when the max is 0), the recipe of "Technical assignment: implement FP8
+    inference on H100" stage 3 step 1 (DelayedScaling(margin, interval))."""
+    h = np.ascontiguousarray(history, dtype=np.float32).ravel()
+    return np.float32(_load().oracle_scale_from_history(_ptr(h), h.size, int(margin)))
 
 
 def quantize_scales_grid(x, dtype, scales) -> np.ndarray:

@@ -37,6 +37,14 @@
  *      multiplied by that block's activation-group scale and weight-block
  *      scale before the blocks are added (the only way both scale grids can
  *      act on one dot product).
+ *   R8 static / delayed scaling ([P1] "Technical assignment: implement FP8
+ *      inference on H100", stage 3 steps 1-2: a calibrated scale, or the
+ *      Transformer Engine recipe DelayedScaling(margin=0, interval=4)): the
+ *      quantizer step is the same E4M3(fl32(x / s)) with the given s (any
+ *      |x / s| > 448 saturates); the next scale from a window of recorded
+ *      amaxes is s = fl32(max / 448) (1 when the max is 0, as R4) times
+ *      2^margin -- a larger margin leaves more headroom, as in the recipe,
+ *      whose quantization multiplier is divided by 2^margin.
  *
  * Layouts: activations A[M][K] and weights W[N][K] are row-major with K
  * contiguous, given as raw 16-bit patterns (FP16 or BF16).  Token-group scales
@@ -347,9 +355,28 @@ void oracle_to_float_array(const uint16_t* x, int dtype, int64_t n, float* out) 
 }
 
 /* The quantizer's elementwise step for a given scale: q = E4M3(fl32(x / s)).
- * Used by exhaustive tests over all 16-bit inputs and many scales. */
+ * It is also the whole static / delayed-scaling quantizer [R8], and serves
+ * the exhaustive tests over all 16-bit inputs and many scales. */
 void oracle_quantize_with_scale(const uint16_t* x, int dtype, int64_t n, float s, uint8_t* q) {
   for (int64_t i = 0; i < n; ++i) q[i] = oracle_e4m3_encode(in_to_float(x[i], dtype) / s);
+}
+
+/* Delayed scaling [R8]: the next dequant factor from H recorded amaxes. */
+float oracle_scale_from_history(const float* h, int64_t H, int margin) {
+  float m = 0.0f;
+  for (int64_t i = 0; i < H; ++i)
+    if (h[i] > m) m = h[i];
+  return ldexpf(scale_of_amax(m), margin);
+}
+
+/* Exact max|x| over n 16-bit inputs, as FP32. */
+float oracle_amax(const uint16_t* x, int dtype, int64_t n) {
+  float m = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float v = fabsf(in_to_float(x[i], dtype));
+    if (v > m) m = v;
+  }
+  return m;
 }
 
 /* Many scales at once: q[j][i] = E4M3(fl32(x[i] / s[j])). */

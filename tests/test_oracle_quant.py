@@ -140,3 +140,77 @@ def test_pseudocode_worked_example(oracle):
     R = oracle.gemm_per_tensor(qa, sa, qw, sw)
     assert abs(R[0, 0] - float(rows["c"][0])) <= 3 * 2.0 ** -24 * 1.5
     assert np.float16(R[0, 0]) == np.float16(1.5)
+
+
+# ------------------------------------------------- static / delayed scaling
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_elementwise_step_arbitrary_scales(oracle, dtype):
+    """A static scale is any FP32 value, not fl32(amax/448): quotients then
+    saturate (|x/s| > 448, including an FP32 overflow to inf), underflow to
+    zero and land anywhere on the E4M3 grid."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = f32(bits, dtype)
+    keep = np.isfinite(x)
+    bits, x = bits[keep], x[keep]
+    rng = np.random.default_rng(123)
+    lo, hi = (-30, 20) if dtype == "f16" else (-120, 120)
+    scales = (2.0 ** rng.uniform(lo, hi, 120)).astype(np.float32)
+    scales = np.concatenate([scales, np.float32([2.0 ** -100, 2.0 ** 95, 0.125, 1.0, 3.0])])
+    got = oracle.quantize_scales_grid(bits, dtype, scales)
+    for j, s in enumerate(scales):
+        assert np.array_equal(got[j], ref_quant(x, s)), f"scale {s!r}"
+    # both saturation and underflow occur for the extreme scales
+    assert np.all(np.isin(got[-5][np.abs(x) > 1e-20], [0x7E, 0xFE]))
+    assert np.all(np.isin(got[-4][np.abs(x) < 2.0 ** 80], [0x00, 0x80]))
+
+
+def _fl32_of_fraction(fr):
+    """The FP32 value nearest to a positive Fraction, ties to even (found by
+    bracketing with numpy's neighbours, independent of any float divide)."""
+    from fractions import Fraction
+    a = np.float32(float(fr))
+    for _ in range(3):
+        lo = np.nextafter(a, np.float32(0))
+        hi = np.nextafter(a, np.float32(np.inf))
+        cands = [lo, a, hi]
+        d = [abs(Fraction(float(c)) - fr) for c in cands]
+        best = min(d)
+        picks = [c for c, dd in zip(cands, d) if dd == best]
+        if len(picks) == 2:
+            picks = [c for c in picks if (int(np.float32(c).view(np.uint32)) & 1) == 0]
+        if picks[0] == a:
+            return a
+        a = picks[0]
+    return a
+
+
+def test_scale_from_history_closed_form(oracle):
+    from fractions import Fraction
+    cases = [([0.5, 3.0, 1.25], 0), ([0.5, 3.0, 1.25], 2), ([0.5, 3.0, 1.25], -3), ([7.0], 0),
+             ([65504.0, 1.0], 1), ([1e-30, 0.0], 0), ([1e30, 2.5], -64), ([0.3, 0.7, 0.1, 0.7], 64)]
+    for hist, margin in cases:
+        h32 = np.float32(hist)
+        m = max(Fraction(float(v)) for v in h32)
+        s0 = _fl32_of_fraction(m / 448)
+        want = Fraction(float(s0)) * Fraction(2) ** margin
+        got = oracle.scale_from_history(h32, margin)
+        assert Fraction(float(got)) == want, (hist, margin, got)
+
+
+def test_scale_from_history_zero_window_and_order(oracle):
+    assert oracle.scale_from_history(np.zeros(5, np.float32), 0) == np.float32(1.0)
+    assert oracle.scale_from_history(np.zeros(5, np.float32), 3) == np.float32(8.0)
+    rng = np.random.default_rng(4)
+    h = (rng.random(64) * 100).astype(np.float32)
+    a = oracle.scale_from_history(h, 1)
+    assert a == oracle.scale_from_history(h[::-1].copy(), 1) == oracle.scale_from_history(np.sort(h), 1)
+    # a window of one equals the dynamic scale of that amax
+    bits = synth.random_bits((31, 17), "f16", seed=21, tensor_id=3, std=4.0)
+    _, s_dyn = oracle.quantize_per_tensor(bits, "f16")
+    assert oracle.scale_from_history(np.float32([oracle.amax(bits, "f16")]), 0) == s_dyn
+
+
+def test_amax_matches_numpy(oracle):
+    for dtype in ("f16", "bf16"):
+        bits = synth.random_bits((3, 1001), dtype, seed=22, tensor_id=4, std=9.0)
+        assert oracle.amax(bits, dtype) == np.abs(f32(bits, dtype)).max()
