@@ -5,6 +5,11 @@ One step = one pass of the whole path over one batch of synthetic input, for
 every linear of the workload and every scaling mode it uses:
   block mode:      token-group quantize of A, block quantize of W, GEMM
   per-tensor mode: per-tensor quantize of A and of W, GEMM
+  per_tensor_static (delayed scaling, opt-in with --modes): A quantized with
+                   the scale held from earlier steps while its amax goes
+                   into a ring of HIST_LEN slots, per-tensor quantize of W,
+                   GEMM, then the next scale from the ring (after the GEMM,
+                   which still needs the scale A was quantized with)
 The two quantizations of a linear are independent: A's runs on a forked
 stream while W's runs on the main one, and the GEMM follows both (the
 fork and join are events inside the captured graph).
@@ -46,6 +51,8 @@ DEFAULT_WORKLOAD = "block_128x4096x4096"
 L2_BYTES_DEFAULT = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
+HIST_LEN = 16        # amax-history ring of the delayed-scaling mode
+HIST_MARGIN = 0      # the recipe's margin (DelayedScaling(margin=0, interval=4))
 
 
 def parse_args():
@@ -58,7 +65,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped to ~2 s")
-    p.add_argument("--modes", default="", help="override the workload's scaling modes, e.g. per_tensor,block")
+    p.add_argument("--modes", default="",
+                   help="override the workload's scaling modes: block, per_tensor, per_tensor_static (comma list)")
     p.add_argument("--profile", type=int, default=0,
                    help="run N eager steps on one input set and exit (a small command for ncu captures)")
     a = p.parse_args()
@@ -89,6 +97,21 @@ def replica_throughput(world, flops_per_step, step_ms):
     return world * flops_per_step / (step_ms * 1e-3) / 1e12
 
 
+def workload_of(args):
+    """The named synthetic workload, with --modes overriding its scaling modes."""
+    import dataclasses
+
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.modes:
+        modes = tuple(args.modes.split(","))
+        bad = [m for m in modes if m not in ("block", "per_tensor", "per_tensor_static")]
+        if bad:
+            raise SystemExit(f"unknown scaling mode(s) {bad}")
+        wl = dataclasses.replace(wl, modes=modes)
+    return wl
+
+
 # ------------------------------------------------------------ algorithmic work
 def kernel_plan(wl):
     """[(linear, mode, [(kernel name, bound, bytes, flops)])] of one step."""
@@ -101,6 +124,11 @@ def kernel_plan(wl):
                       ("quant_weight_block", "hbm", N * K * 3 + 4 * ((N + 127) // 128) * (K // 128), 0),
                       ("gemm_block", None, M * K + N * K + 4 * M * (K // 128) + 4 * ((N + 127) // 128) * (K // 128)
                        + 2 * M * N, 2 * M * N * K)]
+            elif mode == "per_tensor_static":
+                ks = [("quant_static_act", "hbm", M * K * 3 + 8, 0),
+                      ("quant_per_tensor_weight", "hbm", N * K * 3 + 4, 0),
+                      ("gemm_per_tensor", None, M * K + N * K + 8 + 2 * M * N, 2 * M * N * K),
+                      ("scale_from_history", "hbm", 4 * HIST_LEN + 4, 0)]
             else:
                 ks = [("quant_per_tensor_act", "hbm", M * K * 3 + 4, 0),
                       ("quant_per_tensor_weight", "hbm", N * K * 3 + 4, 0),
@@ -260,10 +288,7 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = synth.WORKLOADS[args.workload]
-    if args.modes:
-        import dataclasses
-        wl = dataclasses.replace(wl, modes=tuple(args.modes.split(",")))
+    wl = workload_of(args)
     plan = kernel_plan(wl)
     td = {"f16": torch.float16, "bf16": torch.bfloat16}
     in_t, out_t = td[wl.in_dtype], td[wl.out_dtype]
@@ -307,49 +332,71 @@ def run_ours(args):
             else:
                 b["sa"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
                 b["sw"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
+            if mode == "per_tensor_static":
+                # the held scale starts at the activation's own (calibrated) scale
+                F.fp8_quantize_per_tensor(bufs["a"][lin.K], q=b["qa"], scale=b["sa"])
+                b["hist"] = torch.zeros(HIST_LEN, dtype=torch.float32, device=dev)
             bufs["lin"].append(b)
         sets.append(bufs)
 
-    def kernel_calls(r):
-        """The step's kernels for rotation set r, as zero-argument callables."""
-        calls = []
+    def linear_calls(r):
+        """Per linear of the step for rotation set r: (activation quantize,
+        weight quantize, GEMM, [calls after the GEMM]) as zero-argument
+        callables, in the order of `plan`."""
+        groups = []
         s = sets[r]
         for (lin, mode, ks), b in zip(plan, s["lin"]):
             a = s["a"][lin.K]
             w = s["w"][lin.name]
+            post = []
             if mode == "block":
-                calls.append(lambda a=a, b=b: F.fp8_quantize_token_group(a, q=b["qa"], sa=b["sa"]))
-                calls.append(lambda w=w, b=b: F.fp8_quantize_weight_block(w, q=b["qw"], sb=b["sw"]))
-                calls.append(lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
-                                                           mode="block", c=b["c"]))
+                ca = lambda a=a, b=b: F.fp8_quantize_token_group(a, q=b["qa"], sa=b["sa"])
+                cw = lambda w=w, b=b: F.fp8_quantize_weight_block(w, q=b["qw"], sb=b["sw"])
+                cg = lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
+                                                   mode="block", c=b["c"])
             else:
-                calls.append(lambda a=a, b=b: F.fp8_quantize_per_tensor(a, q=b["qa"], scale=b["sa"]))
-                calls.append(lambda w=w, b=b: F.fp8_quantize_per_tensor(w, q=b["qw"], scale=b["sw"]))
-                calls.append(lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
-                                                           mode="per_tensor", c=b["c"]))
-        return calls
+                if mode == "per_tensor_static":
+                    slot = r % HIST_LEN
+                    ca = lambda a=a, b=b, slot=slot: F.fp8_quantize_per_tensor_static(
+                        a, b["sa"], q=b["qa"], amax=b["hist"][slot:slot + 1])
+                    post = [lambda b=b: F.fp8_scale_from_amax_history(b["hist"], HIST_MARGIN, scale=b["sa"])]
+                else:
+                    ca = lambda a=a, b=b: F.fp8_quantize_per_tensor(a, q=b["qa"], scale=b["sa"])
+                cw = lambda w=w, b=b: F.fp8_quantize_per_tensor(w, q=b["qw"], scale=b["sw"])
+                cg = lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
+                                                   mode="per_tensor", c=b["c"])
+            groups.append((ca, cw, cg, post))
+        return groups
+
+    def kernel_calls(r):
+        """The step's kernels for rotation set r, as zero-argument callables
+        (the order of the kernels in `plan`)."""
+        return [c for ca, cw, cg, post in linear_calls(r) for c in (ca, cw, cg, *post)]
 
     side = torch.cuda.Stream(device=dev)
 
     def run_step(r, main):
         """One step on stream `main`: per linear, the activation is quantized
         on a forked stream while the weight is quantized on `main` (the two
-        are independent), then the GEMM runs on `main` after both."""
-        calls = kernel_calls(r)
-        for i in range(0, len(calls), 3):
+        are independent), then the GEMM runs on `main` after both, followed
+        by the linear's post-GEMM calls (the delayed-scaling update)."""
+        for ca, cw, cg, post in linear_calls(r):
             ev_fork = torch.cuda.Event()
             ev_fork.record(main)
             side.wait_event(ev_fork)
             with torch.cuda.stream(side):
-                calls[i]()
-            calls[i + 1]()
+                ca()
+            cw()
             ev_join = torch.cuda.Event()
             ev_join.record(side)
             main.wait_event(ev_join)
-            calls[i + 2]()
+            cg()
+            for c in post:
+                c()
 
     kinfo = [k for _, _, ks in plan for k in ks]
-    launches_per_kernel = [1 for _ in kinfo]
+    # the static quantizer launches a one-thread kernel that zeroes its amax slot, then the cast kernel
+    launches_per_kernel = [2 if k[0] == "quant_static_act" else 1 for k in kinfo]
 
     # eager warm-up (sets kernel attributes, fills the descriptor cache)
     for r in range(R):
@@ -592,10 +639,17 @@ def oracle_step_sample(wl, gemm_budget_s):
     for lin in wl.linears:
         a, w = acts[lin.K], ws[lin.name]
         for mode in wl.modes:
+            if mode == "per_tensor_static":
+                s_held = oracle.scale_from_history(np.float32([oracle.amax(a, wl.in_dtype)]), 0)
+                hist = np.zeros(HIST_LEN, np.float32)
             t = time.perf_counter()
             if mode == "block":
                 qa, sa = oracle.quantize_token_group(a, wl.in_dtype)
                 qw, sw = oracle.quantize_weight_block(w, wl.in_dtype)
+            elif mode == "per_tensor_static":
+                qa, sa = oracle.quantize_with_scale(a, wl.in_dtype, s_held), s_held
+                hist[0] = oracle.amax(a, wl.in_dtype)
+                qw, sw = oracle.quantize_per_tensor(w, wl.in_dtype)
             else:
                 qa, sa = oracle.quantize_per_tensor(a, wl.in_dtype)
                 qw, sw = oracle.quantize_per_tensor(w, wl.in_dtype)
@@ -608,6 +662,10 @@ def oracle_step_sample(wl, gemm_budget_s):
             else:
                 oracle.gemm_per_tensor(qa, sa, qw, sw, rows=np.arange(rows))
             tg = time.perf_counter() - t
+            if mode == "per_tensor_static":
+                t = time.perf_counter()
+                oracle.scale_from_history(hist, HIST_MARGIN)
+                tq += time.perf_counter() - t
             rate = rows * per_row / max(tg, 1e-9)
             total += tq + tg * lin.M / rows
             parts.append(f"{lin.name}/{mode}: quantize full, GEMM {rows}/{lin.M} rows")
@@ -628,8 +686,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    import synth
-    wl = synth.WORKLOADS[args.workload]
+    wl = workload_of(args)
     flops = sum(2 * lin.M * lin.N * lin.K for lin in wl.linears) * len(wl.modes)
     nlin = len(wl.linears) * len(wl.modes)
     budget = 1.0 / nlin
@@ -646,7 +703,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": args.workload, "description": wl.description},
+        "config": {"workload": args.workload, "description": wl.description, "modes": list(wl.modes)},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.get_threads(), "kind": "oracle",
                          "sample": desc + " (GEMM time extrapolated to all rows)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

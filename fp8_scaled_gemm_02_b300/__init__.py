@@ -4,6 +4,10 @@ Functions carry the names of the C entry points in include/fp8sgemm.h and
 only marshal torch tensors (device memory, current stream) into them:
 
   fp8_quantize_per_tensor(x)            -> (q, scale)        one FP32 scale
+  fp8_quantize_per_tensor_static(x, scale [, amax])
+                                        -> q                 given scale, one read of x
+  fp8_scale_from_amax_history(history, margin)
+                                        -> scale             delayed-scaling update
   fp8_quantize_token_group(x [M,K])     -> (q, sa [K/128,M]) 1x128 groups
   fp8_quantize_weight_block(w [N,K])    -> (q, sb [N/128,K/128]) 128x128 blocks
   fp8_gemm_scaled(qa, sa, qb, sb, ...)  -> C [M,N] FP16/BF16
@@ -22,7 +26,8 @@ from ._lib import (FP8S_BF16, FP8S_F16, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_TENSOR,
                    load, status_string)
 
 __all__ = [
-    "fp8_quantize_per_tensor", "fp8_quantize_token_group", "fp8_quantize_weight_block", "fp8_gemm_scaled",
+    "fp8_quantize_per_tensor", "fp8_quantize_per_tensor_static", "fp8_scale_from_amax_history",
+    "fp8_quantize_token_group", "fp8_quantize_weight_block", "fp8_gemm_scaled",
     "fp8s_device_error", "fp8s_version", "fp8s_gemm_override", "fp8s_gemm_plan", "Fp8sError", "status_string", "load", "LIB_PATH",
     "FP8S_F16", "FP8S_BF16", "FP8S_SCALE_PER_TENSOR", "FP8S_SCALE_BLOCK",
 ]
@@ -63,6 +68,34 @@ def fp8_quantize_per_tensor(x, q=None, scale=None, stream=None):
     st = load().fp8_quantize_per_tensor(_ptr(x), _in_dtype(x), x.numel(), _ptr(q), _ptr(scale), _stream(stream))
     check(st, "fp8_quantize_per_tensor")
     return q, scale
+
+
+def fp8_quantize_per_tensor_static(x, scale, q=None, amax=None, stream=None):
+    """x (any shape, FP16/BF16), scale float32 [1] on the device -> q uint8
+    same shape, q = E4M3(fl32(x / scale)).  `amax` (a float32 CUDA tensor of
+    which the first element is used, e.g. a slot of an amax-history ring)
+    receives max|x|."""
+    _need_cuda(x, scale)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if q is None else q
+    if amax is not None:
+        _need_cuda(amax)
+    st = load().fp8_quantize_per_tensor_static(_ptr(x), _in_dtype(x), x.numel(), _ptr(scale), _ptr(q),
+                                               None if amax is None else _ptr(amax), _stream(stream))
+    check(st, "fp8_quantize_per_tensor_static")
+    return q
+
+
+def fp8_scale_from_amax_history(history, margin=0, scale=None, stream=None):
+    """history float32 [H] (recorded amaxes) -> scale float32 [1] =
+    fl32(max(history) / 448) * 2**margin (1 * 2**margin when the max is 0)."""
+    _need_cuda(history)
+    if history.dtype != torch.float32 or (scale is not None and scale.dtype != torch.float32):
+        raise TypeError("history and scale must be float32")
+    scale = torch.empty(4, dtype=torch.float32, device=history.device)[:1] if scale is None else scale
+    st = load().fp8_scale_from_amax_history(_ptr(history), history.numel(), int(margin), _ptr(scale),
+                                            _stream(stream))
+    check(st, "fp8_scale_from_amax_history")
+    return scale
 
 
 def fp8_quantize_token_group(x, q=None, sa=None, stream=None):

@@ -26,6 +26,8 @@ _I = ctypes.c_int
 # name -> (restype, argtypes); mirrors include/fp8sgemm.h
 SIGNATURES = {
     "fp8_quantize_per_tensor": (_I, [_P, _I, _I64, _P, _P, _P]),
+    "fp8_quantize_per_tensor_static": (_I, [_P, _I, _I64, _P, _P, _P, _P]),
+    "fp8_scale_from_amax_history": (_I, [_P, _I64, _I, _P, _P]),
     "fp8_quantize_token_group": (_I, [_P, _I, _I64, _I64, _P, _P, _P]),
     "fp8_quantize_weight_block": (_I, [_P, _I, _I64, _I64, _P, _P, _P]),
     "fp8_gemm_scaled": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P]),

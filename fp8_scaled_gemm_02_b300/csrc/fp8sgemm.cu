@@ -26,6 +26,7 @@ constexpr int kVersion = 100;  // 0.1.0
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per mbarrier wait
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 inline cudaStream_t as_stream(fp8s_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // Text behind the calling thread's latest FP8S_ERR_CUDA (fp8s_last_cuda_error).
@@ -357,6 +358,42 @@ fp8s_status launch_per_tensor(const void* x, int64_t numel, uint8_t* q, float* s
   return FP8S_OK;
 }
 
+// Per-tensor quantization with a given scale: a grid-stride stream over x,
+// one wave of CTAs (as many as the device holds at once), each thread with
+// kPsUnroll 32-byte units (eight 16-byte loads) in flight.  The amax slot is
+// zeroed first by a one-thread kernel when requested.
+template <int DT>
+fp8s_status launch_static(const void* x, int64_t numel, const float* scale, uint8_t* q, float* amax,
+                          cudaStream_t st, const DeviceInfo& info, int dev) {
+  static std::mutex mu;
+  static int per_sm[kMaxDevices] = {};
+  int resident;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (per_sm[dev] == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_static_kernel<DT>, kPsThreads, 0) != cudaSuccess ||
+          n < 1) {
+        cudaGetLastError();
+        n = 1;
+      }
+      per_sm[dev] = n;
+    }
+    resident = per_sm[dev] * info.sms;
+  }
+  const int64_t nvec = numel / 8;
+  const int ntail = static_cast<int>(numel - nvec * 8);
+  const uint16_t* tail = static_cast<const uint16_t*>(x) + nvec * 8;
+  if (amax) {
+    if (fp8s_status r = launch_ex(zero_word_kernel, 1, 32, 0, st, 1, reinterpret_cast<unsigned int*>(amax))) return r;
+  }
+  const int64_t per_cta = static_cast<int64_t>(kPsThreads) * kPsUnroll * 2;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((nvec + per_cta - 1) / per_cta, resident));
+  return launch_ex(quant_static_kernel<DT>, static_cast<unsigned>(grid), kPsThreads, 0, st, 1,
+                   static_cast<const uint4*>(x), nvec, tail, ntail, scale, reinterpret_cast<uint2*>(q), q + nvec * 8,
+                   reinterpret_cast<unsigned int*>(amax));
+}
+
 // ------------------------------------------------------------------ GEMM
 struct GemmChoice {
   int bn = 128;
@@ -547,6 +584,31 @@ fp8s_status fp8_quantize_per_tensor(const void* x, fp8s_dtype xt, int64_t numel,
   cudaStream_t st = as_stream(stream);
   return xt == FP8S_F16 ? launch_per_tensor<kInF16>(x, numel, q, scale, st, info, dev)
                         : launch_per_tensor<kInBF16>(x, numel, q, scale, st, info, dev);
+}
+
+fp8s_status fp8_quantize_per_tensor_static(const void* x, fp8s_dtype xt, int64_t numel, const float* scale,
+                                           uint8_t* q, float* amax, fp8s_stream_t stream) {
+  if (xt != FP8S_F16 && xt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!x || !q || !scale) return FP8S_ERR_NULL;
+  if (numel < 1) return FP8S_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q) || !aligned4(scale) || !aligned4(amax)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return xt == FP8S_F16 ? launch_static<kInF16>(x, numel, scale, q, amax, st, info, dev)
+                        : launch_static<kInBF16>(x, numel, scale, q, amax, st, info, dev);
+}
+
+fp8s_status fp8_scale_from_amax_history(const float* history, int64_t H, int margin, float* scale,
+                                        fp8s_stream_t stream) {
+  if (!history || !scale) return FP8S_ERR_NULL;
+  if (H < 1 || H > (1LL << 24) || margin < -64 || margin > 64) return FP8S_ERR_SHAPE;
+  if (!aligned4(history) || !aligned4(scale)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  return launch_ex(scale_from_history_kernel, 1, kHsThreads, 0, as_stream(stream), 1, history, H, margin, scale);
 }
 
 fp8s_status fp8_quantize_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K, uint8_t* q, float* sa,

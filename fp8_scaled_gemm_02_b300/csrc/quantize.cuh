@@ -716,4 +716,176 @@ __global__ void __launch_bounds__(kPtThreads, 1)
   if (G > 1) ptx::cluster_wait();
 }
 
+// ------------------------------------------------------------------------
+// K1s: per-tensor quantization with a scale the caller supplies (static or
+// delayed scaling, the Transformer Engine recipe with an amax history):
+// q = E4M3(fl32(x / s)) with s = *scale, one read of x, and optionally the
+// tensor's amax folded into *amax_out (zeroed before the launch; one
+// atomicMax per CTA on the FP32 pattern, which orders like an unsigned
+// integer for non-negative values).
+//
+// The exhaustive check behind the dynamic kernels covers |x| <= 448 s with
+// s = fl32(amax/448) only; here s is arbitrary and |x / s| may saturate, so
+// the double-word quotient q~ = RN(x*y + RN(x*ylo)) is used only with a
+// guard that holds for every s in [2^-90, 2^90]:
+//  * q~ is fl32(x/s) or one of its two FP32 neighbours: y + ylo is 1/s to
+//    about 2^-47 and RN(x*ylo) adds at most 2^-48 relative, far below the
+//    half ulp that separates two roundings;
+//  * two adjacent FP32 values can fall on different E4M3 codes only if one
+//    of them is an E4M3 rounding boundary (a midpoint of the E4M3 grid,
+//    normal or subnormal), and every such boundary has its low 19 mantissa
+//    bits zero (its significand has at most four bits after the leading 1);
+//  * so where some q~ of four elements has low 19 bits 0x7FFFF, 0 or 1, the
+//    four are recomputed with the IEEE divide.  An overflowed q~ (+-inf,
+//    low bits 0) is caught the same way.
+// A power-of-two s has an exact reciprocal (ylo = 0): q~ = x*y is then
+// exactly fl32(x/s) and needs no guard.  Scales outside [2^-90, 2^90]
+// divide every element.
+enum : int { kPsPow2 = 0, kPsGuarded = 1, kPsDivide = 2 };
+constexpr int kPsThreads = 256;
+constexpr int kPsUnroll = 4;  // 32-byte units in flight per thread (eight 16-byte loads)
+
+// (low 19 bits of f's pattern + 1) mod 2^19, moved to the top 19 bits (one
+// IMAD): below 3 << 13 exactly when the low 19 bits are 0x7FFFF, 0 or 1,
+// i.e. when f is on or next to a value whose significand has at most four
+// bits after the leading 1, as every E4M3 rounding boundary has.  (Zeros also land here and take the
+// exact route, as do E4M3-representable quotients: correct, just slower.)
+__device__ __forceinline__ uint32_t boundary_key(float f) { return __float_as_uint(f) * 8192u + 8192u; }
+
+template <int DT>
+__device__ __forceinline__ uint32_t quant4_guarded(uint32_t w0, uint32_t w1, const UnitScale& us,
+                                                   const UnitPair& k) {
+  float q0, q1, q2, q3;
+  ptx::f2_unpack(ptx::f2_fma(unpack2_f2<DT>(w0), k.yy, ptx::f2_mul(unpack2_f2<DT>(w0), k.ll)), q0, q1);
+  ptx::f2_unpack(ptx::f2_fma(unpack2_f2<DT>(w1), k.yy, ptx::f2_mul(unpack2_f2<DT>(w1), k.ll)), q2, q3);
+  const uint32_t key = min(min(boundary_key(q0), boundary_key(q1)), min(boundary_key(q2), boundary_key(q3)));
+  if (__builtin_expect(key < (3u << 13), 0)) {
+    return quant4<DT, true>(w0, w1, us, k);
+  }
+  return __byte_perm(ptx::cvt_e4m3x2(q1, q0), ptx::cvt_e4m3x2(q3, q2), 0x5410) | sign_bytes(w0, w1);
+}
+
+template <int DT, int kPath>
+__device__ __forceinline__ uint2 quant8_static(const uint4& v, const UnitScale& us, const UnitPair& k) {
+  if constexpr (kPath == kPsGuarded) {
+    return make_uint2(quant4_guarded<DT>(v.x, v.y, us, k), quant4_guarded<DT>(v.z, v.w, us, k));
+  } else {
+    return quant8_impl<DT, kPath == kPsDivide>(v, us, k);
+  }
+}
+
+// 16-byte store that does not allocate in L1.
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
+  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// The cast of every 32-byte unit (two input vectors -> one 16-byte output
+// vector), grid-stride; returns this thread's amax pattern.
+template <int DT, int kPath>
+__device__ __forceinline__ uint32_t ps_cast_all(const uint4* __restrict__ x, int64_t nunit, uint4* __restrict__ q,
+                                                const UnitScale& us) {
+  const UnitPair k(us);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kPsThreads;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * kPsThreads + threadIdx.x;
+  uint32_t a = 0;
+  for (; i + (kPsUnroll - 1) * stride < nunit; i += kPsUnroll * stride) {
+    uint4 v[2 * kPsUnroll];
+#pragma unroll
+    for (int u = 0; u < kPsUnroll; ++u) {
+      v[2 * u] = ld_stream(x + 2 * (i + u * stride));
+      v[2 * u + 1] = ld_stream(x + 2 * (i + u * stride) + 1);
+    }
+#pragma unroll
+    for (int u = 0; u < kPsUnroll; ++u) {
+      a = max(a, max(amax_bits8(v[2 * u]), amax_bits8(v[2 * u + 1])));
+      const uint2 lo = quant8_static<DT, kPath>(v[2 * u], us, k);
+      const uint2 hi = quant8_static<DT, kPath>(v[2 * u + 1], us, k);
+      st_stream(q + i + u * stride, make_uint4(lo.x, lo.y, hi.x, hi.y));
+    }
+  }
+  for (; i < nunit; i += stride) {
+    const uint4 v0 = ld_stream(x + 2 * i), v1 = ld_stream(x + 2 * i + 1);
+    a = max(a, max(amax_bits8(v0), amax_bits8(v1)));
+    const uint2 lo = quant8_static<DT, kPath>(v0, us, k);
+    const uint2 hi = quant8_static<DT, kPath>(v1, us, k);
+    st_stream(q + i, make_uint4(lo.x, lo.y, hi.x, hi.y));
+  }
+  return a;
+}
+
+// x: nvec 16-byte vectors (8 elements each) + ntail (< 8) trailing elements;
+// the last vector of an odd nvec and the tail are done by CTA 0.
+template <int DT>
+__global__ void __launch_bounds__(kPsThreads)
+    quant_static_kernel(const uint4* __restrict__ x, int64_t nvec, const uint16_t* __restrict__ tail, int ntail,
+                        const float* __restrict__ scale, uint2* __restrict__ q, uint8_t* __restrict__ q_tail,
+                        unsigned int* __restrict__ amax_out) {
+  __shared__ uint32_t warp_max[kPsThreads / 32];
+  ptx::griddep_wait();
+  const float s = __ldg(scale);
+  const int path = (s >= 0x1p-90f && s <= 0x1p90f) ? ((__float_as_uint(s) & 0x7FFFFFu) == 0 ? kPsPow2 : kPsGuarded)
+                                                   : kPsDivide;
+  const UnitScale us(s, __frcp_rn(s), path == kPsDivide);
+  const int64_t nunit = nvec / 2;
+  uint4* q16 = reinterpret_cast<uint4*>(q);
+  uint32_t a;
+  if (path == kPsPow2) a = ps_cast_all<DT, kPsPow2>(x, nunit, q16, us);
+  else if (path == kPsGuarded) a = ps_cast_all<DT, kPsGuarded>(x, nunit, q16, us);
+  else a = ps_cast_all<DT, kPsDivide>(x, nunit, q16, us);
+  if (blockIdx.x == 0) {
+    if ((nvec & 1) && threadIdx.x == 32) {
+      const uint4 v = ld_stream(x + nvec - 1);
+      a = max(a, amax_bits8(v));
+      q[nvec - 1] = quant8_impl<DT, true>(v, us);
+    }
+    if (threadIdx.x < static_cast<unsigned>(ntail)) {
+      const uint16_t h = tail[threadIdx.x];
+      a = max(a, static_cast<uint32_t>(h & 0x7FFFu));
+      const float t = us.div_exact(unpack2<DT>(static_cast<uint32_t>(h)).x);
+      q_tail[threadIdx.x] =
+          static_cast<uint8_t>(ptx::cvt_e4m3x2(0.0f, t) & 0xFFu) | static_cast<uint8_t>((h >> 8) & 0x80u);
+    }
+  }
+  if (amax_out == nullptr) return;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kPsThreads / 32; ++w) a = max(a, warp_max[w]);
+    atomicMax(amax_out, __float_as_uint(mag_to_float<DT>(a)));
+  }
+}
+
+// Zeroes the amax slot before the static kernel folds its maxima into it.
+// A kernel rather than a memset so that both launches keep programmatic
+// dependent launch (a memset node between them would serialize the stream).
+__global__ void zero_word_kernel(unsigned int* p) {
+  ptx::griddep_wait();
+  *p = 0u;
+}
+
+// Delayed scaling: the next scale from a window of recorded amaxes,
+// s = fl32(max(history) / 448) * 2^margin (1 * 2^margin when the window's
+// maximum is 0).  One CTA.
+constexpr int kHsThreads = 256;
+__global__ void __launch_bounds__(kHsThreads)
+    scale_from_history_kernel(const float* __restrict__ history, int64_t H, int margin, float* __restrict__ scale) {
+  __shared__ float warp_max[kHsThreads / 32];
+  ptx::griddep_wait();
+  float m = 0.0f;
+  for (int64_t i = threadIdx.x; i < H; i += kHsThreads) m = fmaxf(m, history[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kHsThreads / 32; ++w) m = fmaxf(m, warp_max[w]);
+    const float s0 = m == 0.0f ? 1.0f : __fdiv_rn(m, 448.0f);
+    *scale = __fmul_rn(s0, __uint_as_float(static_cast<uint32_t>(127 + margin) << 23));
+  }
+}
+
 }  // namespace fp8s

@@ -10,6 +10,10 @@
  *   [P5] "FP8 chi tiet" (transformers fine-grained FP8 guide), opening
  *        bullets: weights quantized per 128x128 block, activations per token
  *        per group of 128 input channels.
+ * [P1] "Technical assignment: implement FP8 inference on H100" (aivaro.ru,
+ * practice 214), stage 3 steps 1-2, supplies the static/delayed-scaling
+ * variant: a calibrated scale, or one derived from an amax history with a
+ * margin (Transformer Engine's DelayedScaling recipe).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -29,7 +33,9 @@
  *  - E4M3 is the "fn" variant (bias 7, max 448, no infinities); stored
  *    scales are dequantization factors s = fl32(amax / 448) (s = 1 when
  *    amax == 0); q = E4M3_rne_satfinite(fl32(x / s)).
- *  - Every pointer must be 16-byte aligned (FP8S_ERR_ALIGN).
+ *  - Every pointer must be 16-byte aligned (FP8S_ERR_ALIGN), except the
+ *    single floats and the amax history of the static/delayed-scaling
+ *    calls, which need 4-byte alignment.
  */
 #ifndef FP8SGEMM_H
 #define FP8SGEMM_H
@@ -85,6 +91,51 @@ typedef enum {
  */
 FP8S_API fp8s_status fp8_quantize_per_tensor(const void* x, fp8s_dtype xt, int64_t numel,
                                     uint8_t* q, float* scale, fp8s_stream_t stream);
+
+/*
+ * fp8_quantize_per_tensor_static -- static or delayed per-tensor scaling:
+ * [P2] s3 step 4 (q = x / scale rounded to E4M3) with a scale the caller
+ * already holds, so steps 2-3 (amax, scale) leave the critical path and x is
+ * read once.  The scale may come from calibration ([P1] stage 3 step 2,
+ * "Calibrating the FP8 scales") or from an amax history as in the
+ * Transformer Engine recipe DelayedScaling(margin, interval) of [P1] stage 3
+ * step 1 (see fp8_scale_from_amax_history); [P5] "DeepGEMM fast path" names
+ * static activation quantization beside the dynamic scheme.
+ *   x      [numel] FP16/BF16 (xt), device, 16-byte aligned.   numel >= 1.
+ *   scale  one float, device (input, 4-byte aligned): the dequant factor s,
+ *          positive, finite and normal (other values give unspecified bytes,
+ *          never a fault).
+ *   q      [numel] E4M3 bytes, device (output, 16-byte aligned):
+ *          q = E4M3_rne_satfinite(fl32(x / s)); |x / s| above 448 saturates.
+ *   amax   NULL, or one float, device (output, 4-byte aligned): receives
+ *          max|x| over the tensor (exact), e.g. one slot of a ring buffer of
+ *          recorded amaxes.  It is zeroed on `stream` (by a one-thread
+ *          kernel) before the quantize kernel folds in its CTAs' maxima, and
+ *          must not overlap x, q or scale.
+ * One kernel launch (two when amax is given), no memset: both keep
+ * programmatic dependent launch with the stream's neighbouring kernels.
+ */
+FP8S_API fp8s_status fp8_quantize_per_tensor_static(const void* x, fp8s_dtype xt, int64_t numel,
+                                           const float* scale, uint8_t* q, float* amax,
+                                           fp8s_stream_t stream);
+
+/*
+ * fp8_scale_from_amax_history -- the scale update of delayed scaling ([P1]
+ * stage 3 step 1, recipe.DelayedScaling(margin=0, interval=4)):
+ *   s = fl32(max(history[0..H-1]) / 448) * 2^margin   (1 * 2^margin when the
+ *   maximum is 0).
+ *   history  [H] floats, device (input, 4-byte aligned), each >= 0 and
+ *            finite: the amaxes of the last H steps, in any order (a ring
+ *            buffer written by fp8_quantize_per_tensor_static's amax).
+ *            1 <= H <= 2^24.
+ *   margin   -64 <= margin <= 64: powers of two of headroom (a larger margin
+ *            gives a larger dequant factor, so fewer values saturate).
+ *   scale    one float, device (output, 4-byte aligned).
+ * The caller decides how often to call it (the recipe's `interval`: every
+ * interval-th step).  One single-CTA kernel launch.
+ */
+FP8S_API fp8s_status fp8_scale_from_amax_history(const float* history, int64_t H, int margin, float* scale,
+                                        fp8s_stream_t stream);
 
 /*
  * fp8_quantize_token_group -- [P5] per-token 1x128 activation groups, each

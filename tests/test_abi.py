@@ -83,6 +83,28 @@ def test_quantize_argument_checks(lib):
     assert lib.fp8_quantize_per_tensor(GOOD, 0, 10, GOOD, BAD_ALIGN, None) == 3
 
 
+def test_static_scaling_argument_checks(lib):
+    ALIGN4 = P((1 << 20) + 4)   # 4-byte but not 16-byte aligned: enough for single floats
+    q_static = lib.fp8_quantize_per_tensor_static
+    assert q_static(GOOD, 2, 64, GOOD, GOOD, None, None) == 4
+    assert q_static(GOOD, 0, 64, None, GOOD, None, None) == 1
+    assert q_static(None, 0, 64, GOOD, GOOD, None, None) == 1
+    assert q_static(GOOD, 0, 0, GOOD, GOOD, None, None) == 2
+    assert q_static(BAD_ALIGN, 0, 64, GOOD, GOOD, None, None) == 3
+    assert q_static(GOOD, 0, 64, GOOD, BAD_ALIGN, None, None) == 3
+    assert q_static(GOOD, 0, 64, P((1 << 20) + 2), GOOD, None, None) == 3
+    assert q_static(GOOD, 0, 64, GOOD, GOOD, P((1 << 20) + 1), None) == 3
+    hist = lib.fp8_scale_from_amax_history
+    assert hist(None, 4, 0, GOOD, None) == 1
+    assert hist(GOOD, 4, 0, None, None) == 1
+    assert hist(GOOD, 0, 0, GOOD, None) == 2
+    assert hist(GOOD, (1 << 24) + 1, 0, GOOD, None) == 2
+    assert hist(GOOD, 4, 65, GOOD, None) == 2
+    assert hist(GOOD, 4, -65, GOOD, None) == 2
+    assert hist(P((1 << 20) + 2), 4, 0, ALIGN4, None) == 3
+    assert hist(GOOD, 4, 0, P((1 << 20) + 6), None) == 3
+
+
 def test_gemm_argument_checks(lib):
     g = lib.fp8_gemm_scaled
     assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 3, 1, 1, 16, 0, None) == 4          # out dtype
