@@ -65,3 +65,37 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch, capsys):
 
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
+
+
+def test_delayed_scaling_mode_plan():
+    """--modes per_tensor_static: per linear the static activation quantize
+    (two launches: zeroing kernel + cast), the weight quantize, the GEMM and
+    the scale update; the algorithmic bytes count one read of A, one write
+    of q, the scale read and the amax write."""
+    import bench
+
+    class Args:
+        workload = "tinyllama_1.1b_m512"
+        modes = "per_tensor_static"
+
+    wl = bench.workload_of(Args())
+    assert wl.modes == ("per_tensor_static",)
+    plan = bench.kernel_plan(wl)
+    assert len(plan) == len(wl.linears)
+    for lin, mode, ks in plan:
+        names = [k[0] for k in ks]
+        assert names == ["quant_static_act", "quant_per_tensor_weight", "gemm_per_tensor", "scale_from_history"]
+        assert ks[0][2] == lin.M * lin.K * 3 + 8
+        assert ks[3][2] == 4 * bench.HIST_LEN + 4
+        assert ks[2][3] == 2 * lin.M * lin.N * lin.K
+
+
+def test_unknown_mode_is_rejected():
+    import bench
+
+    class Args:
+        workload = "tinyllama_1.1b_m512"
+        modes = "per_tensor,bogus"
+
+    with pytest.raises(SystemExit):
+        bench.workload_of(Args())
