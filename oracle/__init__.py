@@ -56,6 +56,8 @@ def _load():
             "oracle_quantize_with_scale": (None, [P, I, I64, F, P]),
             "oracle_quantize_scales_grid": (None, [P, I, I64, P, I64, P]),
             "oracle_scale_from_history": (F, [P, I64, I]),
+            "oracle_quantize_per_channel": (None, [P, I, I64, I64, P, P]),
+            "oracle_gemm_per_channel": (None, [P, F, P, P, I64, I64, P, I64, P]),
             "oracle_amax": (F, [P, I, I64]),
         }
         for name, (res, args) in sig.items():
@@ -161,6 +163,17 @@ def quantize_weight_block(w, dtype):
     return q, sb
 
 
+def quantize_per_channel(w, dtype):
+    """O3 per output channel (one scale per row of W, "What is FP8 inference
+    on H100" s5): w [N,K] -> (q [N,K], sb [N])."""
+    w = _u16(w)
+    N, K = w.shape
+    q = np.empty((N, K), np.uint8)
+    sb = np.empty(N, np.float32)
+    _load().oracle_quantize_per_channel(_ptr(w), _dt(dtype), N, K, _ptr(q), _ptr(sb))
+    return q, sb
+
+
 def quantize_with_scale(x, dtype, s) -> np.ndarray:
     """The elementwise quantizer step E4M3(fl32(x / s)) for a given scale."""
     x = _u16(x)
@@ -215,6 +228,22 @@ def gemm_per_tensor(qa, sa, qb, sb, rows=None) -> np.ndarray:
     R = np.empty((nr, N), np.float64)
     _load().oracle_gemm_per_tensor(_ptr(qa), float(np.float32(sa)), _ptr(qb), float(np.float32(sb)),
                                    N, K, None if r is None else _ptr(r), nr, _ptr(R))
+    return R
+
+
+def gemm_per_channel(qa, sa, qb, sb, rows=None) -> np.ndarray:
+    """O4 per-channel weights: R = (dec(qa) @ dec(qb)^T) * sa * sb[n] in float64
+    (sa a scalar, sb [N])."""
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qb = np.ascontiguousarray(qb, dtype=np.uint8)
+    sb = np.ascontiguousarray(sb, dtype=np.float32).ravel()
+    M, K = qa.shape
+    N, K2 = qb.shape
+    assert K == K2 and sb.size == N
+    r, nr = _rows(rows, M)
+    R = np.empty((nr, N), np.float64)
+    _load().oracle_gemm_per_channel(_ptr(qa), float(np.float32(sa)), _ptr(qb), _ptr(sb), N, K,
+                                    None if r is None else _ptr(r), nr, _ptr(R))
     return R
 
 

@@ -45,6 +45,11 @@
  *      amaxes is s = fl32(max / 448) (1 when the max is 0, as R4) times
  *      2^margin -- a larger margin leaves more headroom, as in the recipe,
  *      whose quantization multiplier is divided by 2^margin.
+ *   R9 per-channel weight scaling ([P2] s5 "How to minimize the losses":
+ *      per-tensor scaling, or per-channel scaling for weights): one unit per
+ *      output channel, i.e. per row of W[N][K], quantized as in [P2] s3 steps
+ *      2-4; the GEMM multiplies the exact dot product by the activation's
+ *      per-tensor scale and the row's scale.
  *
  * Layouts: activations A[M][K] and weights W[N][K] are row-major with K
  * contiguous, given as raw 16-bit patterns (FP16 or BF16).  Token-group scales
@@ -269,6 +274,24 @@ void oracle_quantize_weight_block(const uint16_t* w, int dtype, int64_t N, int64
   }
 }
 
+/* Per output channel [R9]: one scale per row of W.
+ * w: [N][K]; q: [N][K]; sb: [N]. */
+void oracle_quantize_per_channel(const uint16_t* w, int dtype, int64_t N, int64_t K,
+                                 uint8_t* q, float* sb) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t* row = w + n * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      float v = fabsf(in_to_float(row[k], dtype));
+      if (v > amax) amax = v;
+    }
+    float s = scale_of_amax(amax);
+    for (int64_t k = 0; k < K; ++k) q[n * K + k] = oracle_e4m3_encode(in_to_float(row[k], dtype) / s);
+    sb[n] = s;
+  }
+}
+
 /* ------------------------------------------------------------ O4: GEMM */
 
 static int64_t row_of(const int64_t* rows, int64_t i) { return rows ? rows[i] : i; }
@@ -296,6 +319,24 @@ void oracle_gemm_per_tensor(const uint8_t* qa, float sa, const uint8_t* qb, floa
       for (int64_t k = 0; k < K; ++k)
         acc += dec[qa[m * K + k]] * dec[qb[n * K + k]];
       R[i * N + n] = acc * (double)sa * (double)sb;
+    }
+  }
+}
+
+/* Per-channel weight scales [R9]:
+ *   R[i][n] = (sum_k dec(qa[m][k]) * dec(qb[n][k])) * sa * sb[n],  m = rows[i]. */
+void oracle_gemm_per_channel(const uint8_t* qa, float sa, const uint8_t* qb, const float* sb,
+                             int64_t N, int64_t K, const int64_t* rows, int64_t nrows, double* R) {
+  double dec[256];
+  decode_table(dec);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t m = row_of(rows, i);
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += dec[qa[m * K + k]] * dec[qb[n * K + k]];
+      R[i * N + n] = acc * (double)sa * (double)sb[n];
     }
   }
 }

@@ -137,3 +137,35 @@ def test_tolerance_helper():
     k = int(np.argmax(np.abs(R)))
     Cbad[k] = Cb[k] + np.sign(R[k]) * 2.0 * 2.0 ** (np.frexp(R[k])[1] - 8)
     assert not o.within_tolerance(Cbad, R, "bf16")[0]
+
+
+# ---------------------------------------------------- per-channel weights
+def test_per_channel_vs_fractions(oracle):
+    rng = np.random.default_rng(8)
+    M, N, K = 3, 4, 48
+    qa, qb = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa = np.float32(rng.uniform(0.01, 2))
+    sb = rng.uniform(0.001, 3, N).astype(np.float32)
+    R = oracle.gemm_per_channel(qa, sa, qb, sb)
+    A, B = dec_torch(qa), dec_torch(qb)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(A[m, k])) * Fraction(float(B[n, k])) for k in range(K))
+            exact *= Fraction(float(sa)) * Fraction(float(sb[n]))
+            assert abs(Fraction(float(R[m, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 51)
+
+
+def test_per_channel_scales_columns_not_rows(oracle):
+    """Distinct scales per output column on a non-square shape: a scale applied
+    by row (a swapped index) or a transposed operand fails."""
+    rng = np.random.default_rng(9)
+    M, N, K = 29, 41, 96
+    qa, qb = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sb = (2.0 ** rng.integers(-6, 6, N)).astype(np.float32)   # powers of two: the products stay exact
+    R = oracle.gemm_per_channel(qa, np.float32(0.5), qb, sb)
+    ref = (dec_torch(qa) @ dec_torch(qb).T) * 0.5 * sb[None, :].astype(np.float64)
+    assert np.array_equal(R, ref)
+    # uniform per-channel scales are the per-tensor GEMM
+    u = np.full(N, 1.75, np.float32)
+    assert np.array_equal(oracle.gemm_per_channel(qa, np.float32(0.5), qb, u),
+                          oracle.gemm_per_tensor(qa, np.float32(0.5), qb, np.float32(1.75)))

@@ -214,3 +214,30 @@ def test_amax_matches_numpy(oracle):
     for dtype in ("f16", "bf16"):
         bits = synth.random_bits((3, 1001), dtype, seed=22, tensor_id=4, std=9.0)
         assert oracle.amax(bits, dtype) == np.abs(f32(bits, dtype)).max()
+
+
+# ------------------------------------------------- per-channel weights
+def test_per_channel_is_one_unit_per_row(oracle):
+    for dtype in ("f16", "bf16"):
+        N, K = 37, 640
+        bits = synth.random_bits((N, K), dtype, seed=23, tensor_id=5, std=0.02)
+        # rows of very different magnitude, one all-zero row
+        scale_rows = (2.0 ** (np.arange(N) % 17 - 8)).astype(np.float32)   # 2^-8 .. 2^8
+        x = f32(bits, dtype) * scale_rows[:, None]
+        x[5] = 0.0
+        bits = synth.f32_to_bits(x, dtype)
+        xx = f32(bits, dtype)
+        q, sb = oracle.quantize_per_channel(bits, dtype)
+        want_s = ref_scale(np.abs(xx).max(axis=1))
+        assert np.array_equal(sb, want_s)
+        assert np.array_equal(q, ref_quant(xx, want_s[:, None]))
+        assert sb[5] == 1.0 and not np.any(q[5] & 0x7F)
+
+
+def test_per_channel_with_k128_is_the_token_group_quantizer(oracle):
+    """With K = 128 a row is one 1x128 group: the per-channel quantizer must
+    give the (pinned) token-group quantizer's bytes and scales."""
+    bits = synth.random_bits((50, 128), "bf16", seed=24, tensor_id=6, std=3.0)
+    q1, s1 = oracle.quantize_per_channel(bits, "bf16")
+    q2, s2 = oracle.quantize_token_group(bits, "bf16")
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2[0])
