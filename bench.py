@@ -5,6 +5,8 @@ One step = one pass of the whole path over one batch of synthetic input, for
 every linear of the workload and every scaling mode it uses:
   block mode:      token-group quantize of A, block quantize of W, GEMM
   per-tensor mode: per-tensor quantize of A and of W, GEMM
+  per_channel (opt-in with --modes): per-tensor quantize of A, per-channel
+                   (one scale per output row) quantize of W, GEMM
   per_tensor_static (delayed scaling, opt-in with --modes): A quantized with
                    the scale held from earlier steps while its amax goes
                    into a ring of HIST_LEN slots, per-tensor quantize of W,
@@ -66,7 +68,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped to ~2 s")
     p.add_argument("--modes", default="",
-                   help="override the workload's scaling modes: block, per_tensor, per_tensor_static (comma list)")
+                   help="override the workload's scaling modes: block, per_tensor, per_channel, "
+                        "per_tensor_static (comma list)")
     p.add_argument("--profile", type=int, default=0,
                    help="run N eager steps on one input set and exit (a small command for ncu captures)")
     a = p.parse_args()
@@ -105,7 +108,7 @@ def workload_of(args):
     wl = synth.WORKLOADS[args.workload]
     if args.modes:
         modes = tuple(args.modes.split(","))
-        bad = [m for m in modes if m not in ("block", "per_tensor", "per_tensor_static")]
+        bad = [m for m in modes if m not in ("block", "per_tensor", "per_tensor_static", "per_channel")]
         if bad:
             raise SystemExit(f"unknown scaling mode(s) {bad}")
         wl = dataclasses.replace(wl, modes=modes)
@@ -124,6 +127,10 @@ def kernel_plan(wl):
                       ("quant_weight_block", "hbm", N * K * 3 + 4 * ((N + 127) // 128) * (K // 128), 0),
                       ("gemm_block", None, M * K + N * K + 4 * M * (K // 128) + 4 * ((N + 127) // 128) * (K // 128)
                        + 2 * M * N, 2 * M * N * K)]
+            elif mode == "per_channel":
+                ks = [("quant_per_tensor_act", "hbm", M * K * 3 + 4, 0),
+                      ("quant_per_channel_weight", "hbm", N * K * 3 + 4 * N, 0),
+                      ("gemm_per_channel", None, M * K + N * K + 4 + 4 * N + 2 * M * N, 2 * M * N * K)]
             elif mode == "per_tensor_static":
                 ks = [("quant_static_act", "hbm", M * K * 3 + 8, 0),
                       ("quant_per_tensor_weight", "hbm", N * K * 3 + 4, 0),
@@ -332,6 +339,8 @@ def run_ours(args):
             else:
                 b["sa"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
                 b["sw"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
+            if mode == "per_channel":
+                b["sw"] = torch.empty(N, dtype=torch.float32, device=dev)
             if mode == "per_tensor_static":
                 # the held scale starts at the activation's own (calibrated) scale
                 F.fp8_quantize_per_tensor(bufs["a"][lin.K], q=b["qa"], scale=b["sa"])
@@ -354,6 +363,11 @@ def run_ours(args):
                 cw = lambda w=w, b=b: F.fp8_quantize_weight_block(w, q=b["qw"], sb=b["sw"])
                 cg = lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
                                                    mode="block", c=b["c"])
+            elif mode == "per_channel":
+                ca = lambda a=a, b=b: F.fp8_quantize_per_tensor(a, q=b["qa"], scale=b["sa"])
+                cw = lambda w=w, b=b: F.fp8_quantize_per_channel(w, q=b["qw"], sb=b["sw"])
+                cg = lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
+                                                   mode="per_channel", c=b["c"])
             else:
                 if mode == "per_tensor_static":
                     slot = r % HIST_LEN
@@ -646,6 +660,9 @@ def oracle_step_sample(wl, gemm_budget_s):
             if mode == "block":
                 qa, sa = oracle.quantize_token_group(a, wl.in_dtype)
                 qw, sw = oracle.quantize_weight_block(w, wl.in_dtype)
+            elif mode == "per_channel":
+                qa, sa = oracle.quantize_per_tensor(a, wl.in_dtype)
+                qw, sw = oracle.quantize_per_channel(w, wl.in_dtype)
             elif mode == "per_tensor_static":
                 qa, sa = oracle.quantize_with_scale(a, wl.in_dtype, s_held), s_held
                 hist[0] = oracle.amax(a, wl.in_dtype)
@@ -659,6 +676,8 @@ def oracle_step_sample(wl, gemm_budget_s):
             t = time.perf_counter()
             if mode == "block":
                 oracle.gemm_block(qa, sa, qw, sw, rows=np.arange(rows))
+            elif mode == "per_channel":
+                oracle.gemm_per_channel(qa, sa, qw, sw, rows=np.arange(rows))
             else:
                 oracle.gemm_per_tensor(qa, sa, qw, sw, rows=np.arange(rows))
             tg = time.perf_counter() - t

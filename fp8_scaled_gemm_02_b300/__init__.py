@@ -10,6 +10,7 @@ only marshal torch tensors (device memory, current stream) into them:
                                         -> scale             delayed-scaling update
   fp8_quantize_token_group(x [M,K])     -> (q, sa [K/128,M]) 1x128 groups
   fp8_quantize_weight_block(w [N,K])    -> (q, sb [N/128,K/128]) 128x128 blocks
+  fp8_quantize_per_channel(w [N,K])     -> (q, sb [N])       one scale per output channel
   fp8_gemm_scaled(qa, sa, qb, sb, ...)  -> C [M,N] FP16/BF16
 
 The path is the FP8 linear layer of "What is FP8 inference on H100
@@ -22,21 +23,21 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (FP8S_BF16, FP8S_F16, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_TENSOR, Fp8sError, check,
-                   load, status_string)
+from ._lib import (FP8S_BF16, FP8S_F16, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_CHANNEL, FP8S_SCALE_PER_TENSOR,
+                   Fp8sError, check, load, status_string)
 
 __all__ = [
     "fp8_quantize_per_tensor", "fp8_quantize_per_tensor_static", "fp8_scale_from_amax_history",
-    "fp8_quantize_token_group", "fp8_quantize_weight_block", "fp8_gemm_scaled",
+    "fp8_quantize_token_group", "fp8_quantize_per_channel", "fp8_quantize_weight_block", "fp8_gemm_scaled",
     "fp8s_device_error", "fp8s_version", "fp8s_gemm_override", "fp8s_gemm_plan", "Fp8sError", "status_string", "load", "LIB_PATH",
-    "FP8S_F16", "FP8S_BF16", "FP8S_SCALE_PER_TENSOR", "FP8S_SCALE_BLOCK",
+    "FP8S_F16", "FP8S_BF16", "FP8S_SCALE_PER_TENSOR", "FP8S_SCALE_BLOCK", "FP8S_SCALE_PER_CHANNEL",
 ]
 
 LIB_PATH = _lib.LIB_PATH
 load()  # fail at import time if the CUDA library is missing
 
 _DT = {torch.float16: FP8S_F16, torch.bfloat16: FP8S_BF16}
-_MODE = {"per_tensor": FP8S_SCALE_PER_TENSOR, "block": FP8S_SCALE_BLOCK}
+_MODE = {"per_tensor": FP8S_SCALE_PER_TENSOR, "block": FP8S_SCALE_BLOCK, "per_channel": FP8S_SCALE_PER_CHANNEL}
 
 
 def _stream(stream):
@@ -120,8 +121,21 @@ def fp8_quantize_weight_block(w, q=None, sb=None, stream=None):
     return q, sb
 
 
+def fp8_quantize_per_channel(w, q=None, sb=None, stream=None):
+    """w [N,K] FP16/BF16 -> (q uint8 [N,K], sb float32 [N]): one scale per output channel."""
+    _need_cuda(w)
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
+    sb = torch.empty(N, dtype=torch.float32, device=w.device) if sb is None else sb
+    st = load().fp8_quantize_per_channel(_ptr(w), _in_dtype(w), N, K, _ptr(q), _ptr(sb), _stream(stream))
+    check(st, "fp8_quantize_per_channel")
+    return q, sb
+
+
 def fp8_gemm_scaled(qa, sa, qb, sb, out_dtype=torch.bfloat16, mode="block", c=None, stream=None):
-    """qa [M,K] uint8, qb [N,K] uint8 -> C [M,N] (FP16/BF16) = rescaled qa.qb^T."""
+    """qa [M,K] uint8, qb [N,K] uint8 -> C [M,N] (FP16/BF16) = rescaled qa.qb^T.
+    mode: "per_tensor" (sa, sb one float each), "block" (sa [K/128,M], sb
+    [N/128,K/128]) or "per_channel" (sa one float, sb [N])."""
     _need_cuda(qa, sa, qb, sb)
     M, K = qa.shape
     N = qb.shape[0]

@@ -394,6 +394,38 @@ fp8s_status launch_static(const void* x, int64_t numel, const float* scale, uint
                    reinterpret_cast<unsigned int*>(amax));
 }
 
+// Per-channel weight quantization: persistent CTAs over the rows, each row
+// staged in kvec * 16 bytes of shared memory.
+template <int DT>
+fp8s_status launch_per_channel(const void* w, int64_t N, int64_t K, uint8_t* q, float* sb, cudaStream_t st,
+                               const DeviceInfo& info, int dev) {
+  auto kern = quant_per_channel_kernel<DT>;
+  const int64_t kvec = K / 8;
+  const int smem = static_cast<int>(kvec * 16);
+  static std::mutex mu;
+  static bool attr_done[kMaxDevices] = {};
+  int resident;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (smem > 48 * 1024 && !attr_done[dev]) {
+      if (const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+          e != cudaSuccess)
+        return cuda_fail(e);
+      attr_done[dev] = true;
+    }
+    // CTAs per SM depend on the row's shared memory, so this is asked per call
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kPcThreads, smem) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    resident = n * info.sms;
+  }
+  const int64_t grid = std::min<int64_t>(N, resident);
+  return launch_ex(kern, static_cast<unsigned>(grid), kPcThreads, smem, st, 1, static_cast<const uint4*>(w), N, kvec,
+                   reinterpret_cast<uint2*>(q), sb);
+}
+
 // ------------------------------------------------------------------ GEMM
 struct GemmChoice {
   int bn = 128;
@@ -642,11 +674,29 @@ fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int64_t N, i
                         : launch_weight_block<kInBF16>(w, N, K, q, sb, st, info, dev);
 }
 
+fp8s_status fp8_quantize_per_channel(const void* w, fp8s_dtype wt, int64_t N, int64_t K, uint8_t* q, float* sb,
+                                     fp8s_stream_t stream) {
+  if (wt != FP8S_F16 && wt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!w || !q || !sb) return FP8S_ERR_NULL;
+  if (N < 1 || K < 8 || K % 8 != 0 || K > 65536 || N > (1LL << 31) - 1) return FP8S_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(sb)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return wt == FP8S_F16 ? launch_per_channel<kInF16>(w, N, K, q, sb, st, info, dev)
+                        : launch_per_channel<kInBF16>(w, N, K, q, sb, st, info, dev);
+}
+
 fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, void* c,
-                            fp8s_dtype ct, int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode,
+                            fp8s_dtype ct, int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode_in,
                             fp8s_stream_t stream) {
   if (ct != FP8S_F16 && ct != FP8S_BF16) return FP8S_ERR_DTYPE;
-  if (mode != FP8S_SCALE_PER_TENSOR && mode != FP8S_SCALE_BLOCK) return FP8S_ERR_DTYPE;
+  if (mode_in != FP8S_SCALE_PER_TENSOR && mode_in != FP8S_SCALE_BLOCK && mode_in != FP8S_SCALE_PER_CHANNEL)
+    return FP8S_ERR_DTYPE;
+  // per-channel weights run the per-tensor kernels with a per-column sB
+  const bool per_col = mode_in == FP8S_SCALE_PER_CHANNEL;
+  const fp8s_scale_mode mode = per_col ? FP8S_SCALE_PER_TENSOR : mode_in;
   if (!qa || !sa || !qb || !sb || !c) return FP8S_ERR_NULL;
   if (M < 1 || N < 1 || K < 16 || K % 16 != 0) return FP8S_ERR_SHAPE;
   if (mode == FP8S_SCALE_BLOCK && K % 128 != 0) return FP8S_ERR_SHAPE;
@@ -689,6 +739,9 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
   p.timeout_ns = kWaitTimeoutNs;
 
   auto run = [&](const GemmChoice& c) {
+    if (per_col)
+      return ct == FP8S_F16 ? dispatch_gemm<kModePerChannel, kOutF16>(c, ma, mb, p, info, dev, st)
+                            : dispatch_gemm<kModePerChannel, kOutBF16>(c, ma, mb, p, info, dev, st);
     if (mode == FP8S_SCALE_PER_TENSOR)
       return ct == FP8S_F16 ? dispatch_gemm<kModePerTensor, kOutF16>(c, ma, mb, p, info, dev, st)
                             : dispatch_gemm<kModePerTensor, kOutBF16>(c, ma, mb, p, info, dev, st);
@@ -704,9 +757,11 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
   return r;
 }
 
-fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode, int sms, int* bn, int* splits,
+fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode_in, int sms, int* bn, int* splits,
                            int* pair) {
-  if (mode != FP8S_SCALE_PER_TENSOR && mode != FP8S_SCALE_BLOCK) return FP8S_ERR_DTYPE;
+  if (mode_in != FP8S_SCALE_PER_TENSOR && mode_in != FP8S_SCALE_BLOCK && mode_in != FP8S_SCALE_PER_CHANNEL)
+    return FP8S_ERR_DTYPE;
+  const fp8s_scale_mode mode = mode_in == FP8S_SCALE_PER_CHANNEL ? FP8S_SCALE_PER_TENSOR : mode_in;
   if (!bn || !splits || !pair) return FP8S_ERR_NULL;
   if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || sms < 1) return FP8S_ERR_SHAPE;
   if (mode == FP8S_SCALE_BLOCK && K % 128 != 0) return FP8S_ERR_SHAPE;

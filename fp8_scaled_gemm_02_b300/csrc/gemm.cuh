@@ -70,7 +70,9 @@ constexpr int kBM = 128;   // tile rows = MMA M
 constexpr int kBK = 128;   // K block: 128 E4M3 bytes = one swizzled smem row
 constexpr int kMmaK = 32;  // K of one tcgen05.mma kind::f8f6f4
 
-enum : int { kModePerTensor = 0, kModeBlock = 1 };
+// Per-channel weights (one sB per output column) run the per-tensor kernel
+// with a per-column epilogue scale.
+enum : int { kModePerTensor = 0, kModeBlock = 1, kModePerChannel = 2 };
 enum : int { kOutF16 = 0, kOutBF16 = 1 };
 
 struct GemmParams {
@@ -361,6 +363,20 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
   return true;
 }
 
+// Per-tensor epilogue scaling of CW consecutive columns from n0: by the
+// product sA*sB, or with per-channel weights by sA*sB[n] (the clamped column
+// keeps a ragged tile's loads inside sB; those columns are never stored).
+template <int MODE, int CW>
+__device__ __forceinline__ void scale_chunk(float* v, float pt_scale, float sa, const GemmParams& p, int n0) {
+  if constexpr (MODE == kModePerChannel) {
+#pragma unroll
+    for (int j = 0; j < CW; ++j) v[j] *= sa * __ldg(p.sb + (n0 + j < p.N ? n0 + j : p.N - 1));
+  } else {
+#pragma unroll
+    for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
+  }
+}
+
 template <int BN, int MODE, int OUT, bool SPLIT, bool PAIR>
 __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -576,8 +592,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
     uint32_t unit = 0;
     bool ok = true;
 
-    float pt_scale = 0.0f;
-    if constexpr (MODE == kModePerTensor) pt_scale = __ldg(p.sa) * __ldg(p.sb);
+    float pt_scale = 0.0f, pt_sa = 0.0f;
+    if constexpr (MODE != kModeBlock) {
+      pt_sa = __ldg(p.sa);
+      pt_scale = pt_sa * __ldg(p.sb);
+    }
 
     for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
       int tm, tn;
@@ -586,7 +605,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
       const int n_base = tn * BN + wg * CPT;
       uint16_t* crow = C + static_cast<int64_t>(row) * p.N;
 
-      if constexpr (MODE == kModePerTensor) {
+      if constexpr (MODE != kModeBlock) {
         const uint32_t buf = unit % NBUF;
         if (!ptx::mbar_wait_bounded(&tfull_bar[buf], (unit / NBUF) & 1, p.timeout_ns)) {
           record_error(kErrEpilogue);
@@ -599,8 +618,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
           for (int c = 0; c < CPT / CW; ++c) {
             float v[CW];
             tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
-#pragma unroll
-            for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
+            scale_chunk<MODE, CW>(v, pt_scale, pt_sa, p, n_base + c * CW);
             stage_row<CW>(srow + c * CW, v);
           }
           if (!cluster_waited) {  // peers' barriers are initialised from here on
@@ -615,8 +633,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
           for (int c = 0; c < CPT / CW; ++c) {
             float v[CW];
             tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
-#pragma unroll
-            for (int j = 0; j < CW; ++j) v[j] *= pt_scale;
+            scale_chunk<MODE, CW>(v, pt_scale, pt_sa, p, n_base + c * CW);
             if (row < p.M) store_row<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, v);
           }
         }

@@ -1,11 +1,14 @@
-// quantize.cuh -- dynamic E4M3 quantization kernels (per tensor, per 1x128
-// token group, per 128x128 weight block).
+// quantize.cuh -- E4M3 quantization kernels: dynamic per tensor, per 1x128
+// token group, per 128x128 weight block and per output channel; per tensor
+// with a given (static or delayed) scale.
 //
 // Method ("What is FP8 inference on H100 (Transformer Engine)?", s3 steps
 // 2-4): amax = max|x| over the unit, s = fl32(amax / 448) (1 when amax == 0),
 // q = E4M3_rne_satfinite(fl32(x / s)).  Units are the whole tensor, a group
-// of 128 input channels of one token, or a 128x128 weight block (the
-// transformers "Fine-grained FP8" guide, opening bullets).
+// of 128 input channels of one token, a 128x128 weight block (the
+// transformers "Fine-grained FP8" guide, opening bullets) or one output
+// channel of a weight ("What is FP8 inference on H100", s5: per-channel
+// scaling for weights).
 //
 // All kernels stream 16-byte vectors (8 FP16/BF16 elements) and keep the
 // arithmetic bit-exact with IEEE single precision:
@@ -865,6 +868,48 @@ __global__ void __launch_bounds__(kPsThreads)
 __global__ void zero_word_kernel(unsigned int* p) {
   ptx::griddep_wait();
   *p = 0u;
+}
+
+// ------------------------------------------------------------------------
+// Per output channel (per-channel weight scaling, "What is FP8 inference on
+// H100" s5): one quantization unit per row of W[N][K].  Persistent CTAs take
+// rows in turn; a row (K/8 16-byte vectors) is loaded once into shared
+// memory while its amax is reduced, then cast from there with the row's
+// UnitScale -- the same exact quotient path as the other dynamic
+// quantizers, since every element of a row is within its amax.
+constexpr int kPcThreads = 256;
+
+template <int DT>
+__global__ void __launch_bounds__(kPcThreads)
+    quant_per_channel_kernel(const uint4* __restrict__ w, int64_t N, int64_t kvec, uint2* __restrict__ q,
+                             float* __restrict__ sb) {
+  extern __shared__ uint4 row_s[];
+  __shared__ uint32_t warp_max[kPcThreads / 32];
+  __shared__ uint32_t amax_row;
+  ptx::griddep_wait();
+  for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
+    const uint4* src = w + n * kvec;
+    uint32_t a = 0;
+    for (int64_t i = threadIdx.x; i < kvec; i += kPcThreads) {
+      const uint4 v = ld_stream(src + i);
+      row_s[i] = v;
+      a = max(a, amax_bits8(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int v = 1; v < kPcThreads / 32; ++v) a = max(a, warp_max[v]);
+      amax_row = a;
+    }
+    __syncthreads();
+    const UnitScale us(mag_to_float<DT>(amax_row));
+    uint2* dst = q + n * kvec;
+    for (int64_t i = threadIdx.x; i < kvec; i += kPcThreads) dst[i] = quant8<DT>(row_s[i], us);
+    if (threadIdx.x == 0) sb[n] = us.s;
+    __syncthreads();  // row_s, warp_max and amax_row are reused by the next row
+  }
 }
 
 // Delayed scaling: the next scale from a window of recorded amaxes,

@@ -71,7 +71,8 @@ typedef enum { FP8S_F16 = 0, FP8S_BF16 = 1 } fp8s_dtype;
 
 typedef enum {
   FP8S_SCALE_PER_TENSOR = 0, /* sa, sb each point to one float */
-  FP8S_SCALE_BLOCK = 1       /* sa: [K/128][M] token-group scales, sb: [ceil(N/128)][K/128] block scales */
+  FP8S_SCALE_BLOCK = 1,      /* sa: [K/128][M] token-group scales, sb: [ceil(N/128)][K/128] block scales */
+  FP8S_SCALE_PER_CHANNEL = 2 /* sa: one float (per-tensor activation), sb: [N] one scale per output channel */
 } fp8s_scale_mode;
 
 /*
@@ -138,6 +139,22 @@ FP8S_API fp8s_status fp8_scale_from_amax_history(const float* history, int64_t H
                                         fp8s_stream_t stream);
 
 /*
+ * fp8_quantize_per_channel -- per-channel weight scaling ([P2] s5 "How to
+ * minimize the losses": per-tensor scaling, or per-channel scaling for the
+ * weights): one quantization unit per output channel, i.e. per row of W, each
+ * quantized as in [P2] s3 steps 2-4.  One read of w.
+ *   w   [N][K] FP16/BF16 (wt), device.   N >= 1, 8 <= K <= 65536, K % 8 == 0
+ *       (the GEMM further needs K % 16 == 0).
+ *   q   [N][K] E4M3 bytes, device (output).
+ *   sb  [N] floats, device (output): sb[n] = fl32(max_k |w[n][k]| / 448)
+ *       (1 for an all-zero row).
+ * One kernel launch (persistent CTAs; a row is staged in K*2 bytes of
+ * shared memory).
+ */
+FP8S_API fp8s_status fp8_quantize_per_channel(const void* w, fp8s_dtype wt, int64_t N, int64_t K,
+                                     uint8_t* q, float* sb, fp8s_stream_t stream);
+
+/*
  * fp8_quantize_token_group -- [P5] per-token 1x128 activation groups, each
  * group quantized as in [P2] s3 steps 2-4.  One read of x.
  *   x   [M][K] FP16/BF16 (xt), device.   M >= 1, K >= 128, K % 128 == 0.
@@ -172,6 +189,10 @@ FP8S_API fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int
  *        [ceil(N/128)][K/128]; each 128-wide K block's FP32 partial sum is
  *        multiplied by sa[kb][m] * sb[n/128][kb] and added into an FP32
  *        accumulator;  C[m][n] = RN(acc).             K % 128 == 0.
+ *   mode FP8S_SCALE_PER_CHANNEL ([P2] s5 per-channel weight scaling): sa ->
+ *        one float, sb [N] (from fp8_quantize_per_channel);
+ *        C[m][n] = RN(acc[m][n] * (sa * sb[n])).       K % 16 == 0.
+ *        The same kernels and tiles as per-tensor mode.
  *   M, N >= 1, K >= 16.  N need not be a multiple of anything.
  */
 FP8S_API fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,

@@ -83,6 +83,27 @@ def test_quantize_argument_checks(lib):
     assert lib.fp8_quantize_per_tensor(GOOD, 0, 10, GOOD, BAD_ALIGN, None) == 3
 
 
+def test_per_channel_argument_checks(lib):
+    pc = lib.fp8_quantize_per_channel
+    assert pc(GOOD, 3, 4, 128, GOOD, GOOD, None) == 4
+    assert pc(GOOD, 0, 4, 128, None, GOOD, None) == 1
+    assert pc(GOOD, 0, 0, 128, GOOD, GOOD, None) == 2
+    assert pc(GOOD, 0, 4, 12, GOOD, GOOD, None) == 2          # K % 8
+    assert pc(GOOD, 0, 4, 65544, GOOD, GOOD, None) == 2       # a row must fit in 128 KB of shared memory
+    assert pc(GOOD, 1, 4, 128, GOOD, BAD_ALIGN, None) == 3
+    # the GEMM's per-channel mode: same shape rules as per-tensor (K % 16, not K % 128)
+    g = lib.fp8_gemm_scaled
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 8, 8, 24, 2, None) == 2
+    assert g(GOOD, GOOD, GOOD, BAD_ALIGN, GOOD, 0, 8, 8, 32, 2, None) == 3
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 8, 8, 32, 3, None) == 4
+
+
+def test_per_channel_plan_is_the_per_tensor_plan(lib):
+    from fp8_scaled_gemm_02_b300 import fp8s_gemm_plan
+    for M, N, K in [(128, 4096, 4096), (512, 2560, 2048), (4096, 22016, 4096), (64, 64, 128)]:
+        assert fp8s_gemm_plan(M, N, K, "per_channel") == fp8s_gemm_plan(M, N, K, "per_tensor")
+
+
 def test_static_scaling_argument_checks(lib):
     ALIGN4 = P((1 << 20) + 4)   # 4-byte but not 16-byte aligned: enough for single floats
     q_static = lib.fp8_quantize_per_tensor_static

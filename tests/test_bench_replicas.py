@@ -99,3 +99,17 @@ def test_unknown_mode_is_rejected():
 
     with pytest.raises(SystemExit):
         bench.workload_of(Args())
+
+
+def test_per_channel_mode_plan():
+    import bench
+
+    class Args:
+        workload = "llama2_7b_m128"
+        modes = "per_channel"
+
+    plan = bench.kernel_plan(bench.workload_of(Args()))
+    for lin, mode, ks in plan:
+        assert [k[0] for k in ks] == ["quant_per_tensor_act", "quant_per_channel_weight", "gemm_per_channel"]
+        assert ks[1][2] == lin.N * lin.K * 3 + 4 * lin.N
+        assert ks[2][2] == lin.M * lin.K + lin.N * lin.K + 4 + 4 * lin.N + 2 * lin.M * lin.N
