@@ -61,6 +61,13 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _need_f32(*ts):
+    """Scales, amaxes and histories are read and written as raw FP32 words."""
+    for t in ts:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"scale / amax / history tensors must be float32, got {t.dtype}")
+
+
 def fp8_quantize_per_tensor(x, q=None, scale=None, stream=None):
     """x (any shape, FP16/BF16) -> (q uint8 same shape, scale float32 [1])."""
     _need_cuda(x)
@@ -77,6 +84,7 @@ def fp8_quantize_per_tensor_static(x, scale, q=None, amax=None, stream=None):
     which the first element is used, e.g. a slot of an amax-history ring)
     receives max|x|."""
     _need_cuda(x, scale)
+    _need_f32(scale, amax)
     q = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if q is None else q
     if amax is not None:
         _need_cuda(amax)
@@ -90,8 +98,7 @@ def fp8_scale_from_amax_history(history, margin=0, scale=None, stream=None):
     """history float32 [H] (recorded amaxes) -> scale float32 [1] =
     fl32(max(history) / 448) * 2**margin (1 * 2**margin when the max is 0)."""
     _need_cuda(history)
-    if history.dtype != torch.float32 or (scale is not None and scale.dtype != torch.float32):
-        raise TypeError("history and scale must be float32")
+    _need_f32(history, scale)
     scale = torch.empty(4, dtype=torch.float32, device=history.device)[:1] if scale is None else scale
     st = load().fp8_scale_from_amax_history(_ptr(history), history.numel(), int(margin), _ptr(scale),
                                             _stream(stream))
@@ -127,6 +134,7 @@ def fp8_quantize_per_channel(w, q=None, sb=None, stream=None):
     N, K = w.shape
     q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
     sb = torch.empty(N, dtype=torch.float32, device=w.device) if sb is None else sb
+    _need_f32(sb)
     st = load().fp8_quantize_per_channel(_ptr(w), _in_dtype(w), N, K, _ptr(q), _ptr(sb), _stream(stream))
     check(st, "fp8_quantize_per_channel")
     return q, sb
