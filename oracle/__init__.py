@@ -57,6 +57,10 @@ def _load():
             "oracle_quantize_scales_grid": (None, [P, I, I64, P, I64, P]),
             "oracle_scale_from_history": (F, [P, I64, I]),
             "oracle_quantize_per_channel": (None, [P, I, I64, I64, P, P]),
+            "oracle_ue8m0_decode": (F, [ctypes.c_uint8]),
+            "oracle_ue8m0_of_amax": (ctypes.c_uint8, [F]),
+            "oracle_quantize_token_group_ue8m0": (None, [P, I, I64, I64, P, P]),
+            "oracle_quantize_weight_block_ue8m0": (None, [P, I, I64, I64, P, P]),
             "oracle_gemm_per_channel": (None, [P, F, P, P, I64, I64, P, I64, P]),
             "oracle_amax": (F, [P, I, I64]),
         }
@@ -172,6 +176,41 @@ def quantize_per_channel(w, dtype):
     sb = np.empty(N, np.float32)
     _load().oracle_quantize_per_channel(_ptr(w), _dt(dtype), N, K, _ptr(q), _ptr(sb))
     return q, sb
+
+
+def ue8m0_decode(codes) -> np.ndarray:
+    """UE8M0 scale codes -> float32 values 2^(c - 127) (255 -> NaN)."""
+    c = np.asarray(codes, np.uint8)
+    lib = _load()
+    return np.array([lib.oracle_ue8m0_decode(int(v)) for v in c.ravel()], np.float32).reshape(c.shape)
+
+
+def ue8m0_of_amax(amax) -> int:
+    """The UE8M0 code of the power-of-two scale for an amax: fl32(amax/448)
+    rounded up to a power of two (1 when amax == 0), clamped to 2^-127."""
+    return int(_load().oracle_ue8m0_of_amax(float(np.float32(amax))))
+
+
+def quantize_token_group_ue8m0(x, dtype):
+    """Token-group quantizer with UE8M0 scales: x [M,K] -> (q [M,K], codes [K/128, M])."""
+    x = _u16(x)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), np.uint8)
+    c = np.empty((K // 128, M), np.uint8)
+    _load().oracle_quantize_token_group_ue8m0(_ptr(x), _dt(dtype), M, K, _ptr(q), _ptr(c))
+    return q, c
+
+
+def quantize_weight_block_ue8m0(w, dtype):
+    """Weight-block quantizer with UE8M0 scales: w [N,K] -> (q [N,K], codes [ceil(N/128), K/128])."""
+    w = _u16(w)
+    N, K = w.shape
+    assert K % 128 == 0
+    q = np.empty((N, K), np.uint8)
+    c = np.empty(((N + 127) // 128, K // 128), np.uint8)
+    _load().oracle_quantize_weight_block_ue8m0(_ptr(w), _dt(dtype), N, K, _ptr(q), _ptr(c))
+    return q, c
 
 
 def quantize_with_scale(x, dtype, s) -> np.ndarray:

@@ -45,6 +45,14 @@
  *      amaxes is s = fl32(max / 448) (1 when the max is 0, as R4) times
  *      2^margin -- a larger margin leaves more headroom, as in the recipe,
  *      whose quantization multiplier is divided by 2^margin.
+ *   R10 UE8M0 scales ([P5] "UE8M0 scale format": DeepSeek-V4-style
+ *      checkpoints keep FP8 weight scales as packed float8_e8m0fnu, and the
+ *      Blackwell DeepGEMM kernels take only such scales): a scale is a power
+ *      of two 2^(c - 127) stored as its biased exponent byte c (c = 255 is
+ *      NaN).  The quantizer first takes the FP32 scale of R2/R4,
+ *      fl32(amax / 448), then rounds it UP to a power of two (so no element
+ *      exceeds 448 by more than that FP32 rounding), clamped to 2^-127, the
+ *      smallest UE8M0 value; x / s is then an exact power-of-two division.
  *   R9 per-channel weight scaling ([P2] s5 "How to minimize the losses":
  *      per-tensor scaling, or per-channel scaling for weights): one unit per
  *      output channel, i.e. per row of W[N][K], quantized as in [P2] s3 steps
@@ -289,6 +297,70 @@ void oracle_quantize_per_channel(const uint16_t* w, int dtype, int64_t N, int64_
     float s = scale_of_amax(amax);
     for (int64_t k = 0; k < K; ++k) q[n * K + k] = oracle_e4m3_encode(in_to_float(row[k], dtype) / s);
     sb[n] = s;
+  }
+}
+
+/* UE8M0 [R10]: the value of a scale code, and the code of the power-of-two
+ * scale that a dynamic quantizer uses for a given amax. */
+float oracle_ue8m0_decode(uint8_t c) {
+  if (c == 0xFF) return f32_of_bits(0x7FC00000u);
+  return ldexpf(1.0f, (int)c - 127);
+}
+
+uint8_t oracle_ue8m0_of_amax(float amax) {
+  float s = scale_of_amax(amax);             /* fl32(amax / 448), 1 when amax == 0 */
+  int e;
+  float m = frexpf(s, &e);                   /* s = m * 2^e, m in [0.5, 1) */
+  int k = (m == 0.5f) ? e - 1 : e;           /* the smallest k with 2^k >= s */
+  if (k < -127) k = -127;
+  return (uint8_t)(k + 127);
+}
+
+/* Token-group and weight-block quantizers with UE8M0 scales [R10]: as the
+ * FP32-scale ones, with s replaced by its power-of-two round-up.  The scales
+ * are returned as codes; their values are oracle_ue8m0_decode(code). */
+void oracle_quantize_token_group_ue8m0(const uint16_t* x, int dtype, int64_t M, int64_t K,
+                                       uint8_t* q, uint8_t* sa_code) {
+  int64_t G = K / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t g = 0; g < G; ++g) {
+      const uint16_t* row = x + m * K + g * 128;
+      float amax = 0.0f;
+      for (int k = 0; k < 128; ++k) {
+        float v = fabsf(in_to_float(row[k], dtype));
+        if (v > amax) amax = v;
+      }
+      uint8_t c = oracle_ue8m0_of_amax(amax);
+      float s = oracle_ue8m0_decode(c);
+      for (int k = 0; k < 128; ++k) q[m * K + g * 128 + k] = oracle_e4m3_encode(in_to_float(row[k], dtype) / s);
+      sa_code[g * M + m] = c;
+    }
+  }
+}
+
+void oracle_quantize_weight_block_ue8m0(const uint16_t* w, int dtype, int64_t N, int64_t K,
+                                        uint8_t* q, uint8_t* sb_code) {
+  int64_t NB = (N + 127) / 128;
+  int64_t KB = K / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t bi = 0; bi < NB; ++bi) {
+    for (int64_t bj = 0; bj < KB; ++bj) {
+      int64_t r0 = bi * 128;
+      int64_t r1 = r0 + 128 < N ? r0 + 128 : N;
+      float amax = 0.0f;
+      for (int64_t r = r0; r < r1; ++r)
+        for (int64_t c = bj * 128; c < bj * 128 + 128; ++c) {
+          float v = fabsf(in_to_float(w[r * K + c], dtype));
+          if (v > amax) amax = v;
+        }
+      uint8_t code = oracle_ue8m0_of_amax(amax);
+      float s = oracle_ue8m0_decode(code);
+      for (int64_t r = r0; r < r1; ++r)
+        for (int64_t c = bj * 128; c < bj * 128 + 128; ++c)
+          q[r * K + c] = oracle_e4m3_encode(in_to_float(w[r * K + c], dtype) / s);
+      sb_code[bi * KB + bj] = code;
+    }
   }
 }
 
