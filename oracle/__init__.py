@@ -58,6 +58,8 @@ def _load():
             "oracle_scale_from_history": (F, [P, I64, I]),
             "oracle_quantize_per_channel": (None, [P, I, I64, I64, P, P]),
             "oracle_ue8m0_decode": (F, [ctypes.c_uint8]),
+            "oracle_e5m2_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "oracle_e5m2_encode_array": (None, [P, I64, P]),
             "oracle_ue8m0_of_amax": (ctypes.c_uint8, [F]),
             "oracle_quantize_token_group_ue8m0": (None, [P, I, I64, I64, P, P]),
             "oracle_quantize_weight_block_ue8m0": (None, [P, I, I64, I64, P, P]),
@@ -176,6 +178,21 @@ def quantize_per_channel(w, dtype):
     sb = np.empty(N, np.float32)
     _load().oracle_quantize_per_channel(_ptr(w), _dt(dtype), N, K, _ptr(q), _ptr(sb))
     return q, sb
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    """E5M2 codes (5 exponent + 2 mantissa bits, bias 15) -> float64."""
+    c = np.asarray(codes, np.uint8)
+    lib = _load()
+    return np.array([lib.oracle_e5m2_decode(int(v)) for v in c.ravel()], np.float64).reshape(c.shape)
+
+
+def e5m2_encode(y) -> np.ndarray:
+    """float32 -> E5M2 codes, round to nearest even, saturating at +-57344."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.empty(y.shape, np.uint8)
+    _load().oracle_e5m2_encode_array(_ptr(y), y.size, _ptr(out))
+    return out
 
 
 def ue8m0_decode(codes) -> np.ndarray:

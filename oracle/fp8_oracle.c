@@ -53,6 +53,11 @@
  *      fl32(amax / 448), then rounds it UP to a power of two (so no element
  *      exceeds 448 by more than that FP32 rounding), clamped to 2^-127, the
  *      smallest UE8M0 value; x / s is then an exact power-of-two division.
+ *   R11 E5M2 ([P2] s2: 5 exponent + 2 mantissa bits, the format named for
+ *      gradients; [P3] s2 the same split): the IEEE-style layout, bias 15,
+ *      S.11111.00 = infinity, S.11111.xx (xx != 0) = NaN, largest finite
+ *      value 1.75 * 2^15 = 57344; encoding rounds to nearest even and, like
+ *      the E4M3 path, saturates finite overflow (and infinities) to +-57344.
  *   R9 per-channel weight scaling ([P2] s5 "How to minimize the losses":
  *      per-tensor scaling, or per-channel scaling for weights): one unit per
  *      output channel, i.e. per row of W[N][K], quantized as in [P2] s3 steps
@@ -203,6 +208,69 @@ uint8_t oracle_e4m3_encode(float y) {
   }
   if (code > 0x7E) code = 0x7E; /* 480 does not exist in E4M3 fn */
   return (uint8_t)(sign | code);
+}
+
+/* ----------------------------------------------------- E5M2 codec [R11] */
+
+double oracle_e5m2_decode(uint8_t b) {
+  int sign = b >> 7;
+  int E = (b >> 2) & 31;
+  int m = b & 3;
+  double v;
+  if (E == 31) {
+    if (m != 0) return NAN;
+    v = INFINITY;
+  } else if (E == 0) {
+    v = ldexp((double)m, -16); /* subnormal: m * 2^-2 * 2^-14 */
+  } else {
+    v = ldexp(1.0 + m / 4.0, E - 15);
+  }
+  return sign ? -v : v;
+}
+
+/* Round-to-nearest-even onto the E5M2 grid with saturation to +-57344; the
+ * same exact integer method as the E4M3 encoder (grid step 2^(e - 2) in the
+ * normal binades, 2^-16 below 2^-14). */
+uint8_t oracle_e5m2_encode(float y) {
+  uint32_t u = bits_of_f32(y);
+  uint8_t sign = (uint8_t)((u >> 31) << 7);
+  uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint8_t)(sign | 0x7F); /* NaN */
+  if (a >= 0x47700000u) return (uint8_t)(sign | 0x7B); /* |y| >= 61440 = (57344 + 65536) / 2, incl. inf */
+  int ebits = (int)(a >> 23);
+  if (ebits == 0) return sign; /* binary32 subnormal or zero: far below 2^-17 */
+  uint64_t mant = (uint64_t)((a & 0x7FFFFFu) | 0x800000u);
+  int e = ebits - 127;
+  int ee = e < -14 ? -14 : e;
+  int shift = 21 + (ee - e); /* |y| / 2^(ee - 2) = mant * 2^(e - 23 - ee + 2) */
+  uint64_t n;
+  if (shift >= 40) {
+    n = 0;
+  } else {
+    uint64_t q = mant >> shift;
+    uint64_t rem = mant & ((1ull << shift) - 1ull);
+    uint64_t half = 1ull << (shift - 1);
+    if (rem > half || (rem == half && (q & 1ull))) q += 1;
+    n = q;
+  }
+  /* value = n * 2^(ee - 2); n <= 8 */
+  if (n == 0) return sign;
+  if (n == 8) { /* carry into the next binade */
+    n = 4;
+    ee += 1;
+  }
+  int code;
+  if (n < 4) {
+    code = (int)n; /* ee == -14: E5M2 subnormal */
+  } else {
+    code = ((ee + 15) << 2) | (int)(n - 4);
+  }
+  if (code > 0x7B) code = 0x7B; /* above 57344 only infinity remains: saturate */
+  return (uint8_t)(sign | code);
+}
+
+void oracle_e5m2_encode_array(const float* y, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e5m2_encode(y[i]);
 }
 
 /* --------------------------------------------------- O3: the quantizers */
