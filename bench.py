@@ -27,11 +27,19 @@ both sides, max over ranks):
                  launches (rotating input sets) in one CUDA graph between two
                  events; these per-launch durations feed `roofline` and
                  `kernels`.
-  e2e region:    K steps through the public API with host buffers: H2D of A
-                 and W from pinned memory, the path, D2H of C.
+  e2e region:    K steps (capped to ~2 s) through the public API with host
+                 buffers: per step, H2D of A and W from pinned memory, the
+                 path, D2H of C; consecutive steps overlap their uploads,
+                 compute and read-backs on three streams.
 
 `--impl reference` times the CPU oracle (the plain C reference of the same
-path) on the host cores, on a bounded sample of the same workload.
+path) on the host cores, on a bounded sample of the same workload: every
+quantizer in full and the first rows of each GEMM (ORACLE_SAMPLE_FLOP in
+all), extrapolated to all rows; the median over the sampled steps.  The GPU
+arm's `cpu_baseline` times the same sample (median of 3 after one warm-up).
+
+The default workload is the largest one (16384x8192 outlier activations
+times an 8192x8192 weight, block-scaled).
 """
 import argparse
 import hashlib
@@ -49,7 +57,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "FP8 scaled-GEMM TFLOP/s & % of dense FP8 peak; quantize GB/s & % of HBM peak"
-DEFAULT_WORKLOAD = "block_128x4096x4096"
+DEFAULT_WORKLOAD = "outlier_16384x8192x8192"   # the largest workload: the block-scaled GEMM at scale
 L2_BYTES_DEFAULT = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
@@ -60,7 +68,7 @@ HIST_MARGIN = 0      # the recipe's margin (DelayedScaling(margin=0, interval=4)
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30000)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -113,6 +121,16 @@ def workload_of(args):
             raise SystemExit(f"unknown scaling mode(s) {bad}")
         wl = dataclasses.replace(wl, modes=modes)
     return wl
+
+
+def config_of(args, wl):
+    """The `config` object of the JSON line, identical in both arms."""
+    return {"workload": args.workload, "description": wl.description,
+            "linears": [[lin.name, lin.M, lin.N, lin.K] for lin in wl.linears], "modes": list(wl.modes),
+            "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype,
+            "l2": "defeated: the GPU arm rotates over enough input sets that consecutive uses of one set are "
+                  "more than 2x the L2 size apart",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
 # ------------------------------------------------------------ algorithmic work
@@ -516,40 +534,73 @@ def run_ours(args):
     if not args.no_e2e:
         pin_a = {k: to_t(v).pin_memory() for k, v in host_a.items()}
         pin_w = {k: to_t(v).pin_memory() for k, v in host_w.items()}
-        pin_c = [torch.empty((lin.M, lin.N), dtype=out_t).pin_memory() for lin, _, _ in plan]
+        # one pinned output buffer per linear and input set, so that the
+        # read-back of step i never shares host memory with that of step i+1
+        pin_c = [[torch.empty((lin.M, lin.N), dtype=out_t).pin_memory() for lin, _, _ in plan] for _ in range(R)]
         h2d = sum(t.numel() * 2 for t in pin_a.values()) + sum(t.numel() * 2 for t in pin_w.values())
-        d2h = sum(t.numel() * 2 for t in pin_c)
+        d2h = sum(t.numel() * 2 for t in pin_c[0])
+        up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(R)]      # set r's inputs have landed
+        ev_done = [torch.cuda.Event() for _ in range(R)]    # set r's step has finished
+        ev_out = [torch.cuda.Event() for _ in range(R)]     # set r's outputs have been read back
+        used = [False] * R
 
-        def e2e_step(r):
+        def e2e_step(i):
+            """Step i on input set r = i % R, pipelined over three streams: the
+            upload of step i+1 and the read-back of step i-1 overlap the
+            compute of step i.  A set is re-uploaded only after its previous
+            step finished, and recomputed only after its previous outputs
+            were read back."""
+            r = i % R
             s = sets[r]
-            for k, t in pin_a.items():
-                s["a"][k].copy_(t, non_blocking=True)
-            for k, t in pin_w.items():
-                s["w"][k].copy_(t, non_blocking=True)
+            if used[r]:
+                up.wait_event(ev_done[r])
+            with torch.cuda.stream(up):
+                for k, t in pin_a.items():
+                    s["a"][k].copy_(t, non_blocking=True)
+                for k, t in pin_w.items():
+                    s["w"][k].copy_(t, non_blocking=True)
+                ev_in[r].record(up)
+            stream.wait_event(ev_in[r])
+            if used[r]:
+                stream.wait_event(ev_out[r])
             run_step(r, stream)
-            for b, hc in zip(s["lin"], pin_c):
-                hc.copy_(b["c"], non_blocking=True)
+            ev_done[r].record(stream)
+            down.wait_event(ev_done[r])
+            with torch.cuda.stream(down):
+                for b, hc in zip(s["lin"], pin_c[r]):
+                    hc.copy_(b["c"], non_blocking=True)
+                ev_out[r].record(down)
+            used[r] = True
 
         with torch.cuda.stream(stream):
             for i in range(W):
-                e2e_step(i % R)
+                e2e_step(i)
             barrier()
             ke = args.e2e_steps or K
             probe0 = time.perf_counter()
             e2e_step(0)
-            stream.synchronize()
+            torch.cuda.synchronize()
             per = max(time.perf_counter() - probe0, 1e-6)
             ke = max(3, min(ke, int(2.0 / per)))
+            barrier()
             ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ea.record(stream)
+            ea.record(up)   # every stream is idle here: the region starts with the first upload
+            stream.wait_event(ea)
+            down.wait_event(ea)
             for i in range(ke):
-                e2e_step(i % R)
-            eb.record(stream)
+                e2e_step(i)
+            last = torch.cuda.Event()
+            last.record(down)
+            stream.wait_event(last)
+            eb.record(stream)   # after the last read-back
             barrier()
             e2e_ms = rank_max(ea.elapsed_time(eb)) / ke
         flops_step = sum(k[3] for k in kinfo)
         e2e = {"value": round(replica_throughput(world, flops_step, e2e_ms), 4), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": round(e2e_ms, 5)}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": round(e2e_ms, 5),
+               "copies": "pinned host buffers; uploads, compute and read-backs of consecutive steps overlap on "
+                         "three streams"}
 
     # ---- numbers
     peaks, peaks_src = load_peaks()
@@ -599,11 +650,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(step_ms, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate", "data": "synthetic (seeded Philox normal / Student-t inputs)",
-        "config": {"workload": args.workload, "description": wl.description,
-                   "linears": [[lin.name, lin.M, lin.N, lin.K] for lin in wl.linears], "modes": list(wl.modes),
-                   "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype,
-                   "l2": f"rotating {R} input sets ({R * set_bytes / 1e6:.0f} MB; L2 {l2 / 1e6:.0f} MB)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": config_of(args, wl),
+        "l2_rotation": f"{R} input sets ({R * set_bytes / 1e6:.0f} MB; L2 {l2 / 1e6:.0f} MB)",
         "roofline": roof,
         "kernels": kernels,
         "kernel_region": {"steps": Kk, "ms_per_step": round(kregion_step_ms, 6),
@@ -614,7 +662,7 @@ def run_ours(args):
         "clocks": sampler.summary(t0, t1, t_wide0),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, budget_s=8.0)
+        line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -638,9 +686,23 @@ def workload_inputs(wl):
     return _INPUTS[wl.name]
 
 
-def oracle_step_sample(wl, gemm_budget_s):
+# FLOPs of oracle GEMM work in one sampled step (split evenly over the step's
+# GEMMs; each GEMM runs its first rows and is extrapolated to all M rows).
+# Fixed, so that the GPU arm's cpu_baseline and the reference arm time the
+# same sample and report the same rate.
+ORACLE_SAMPLE_FLOP = 2e10
+
+
+def oracle_sample_rows(wl):
+    """Rows of each GEMM in the sampled oracle step, in `kernel_plan` order."""
+    nlin = len(wl.linears) * len(wl.modes)
+    share = ORACLE_SAMPLE_FLOP / nlin
+    return [int(max(1, min(lin.M, round(share / (2 * lin.N * lin.K))))) for lin in wl.linears for _ in wl.modes]
+
+
+def oracle_step_sample(wl):
     """Times the oracle on one pass of the workload: every quantizer in full
-    and, per GEMM, the first r rows (r sized to the time budget), extrapolated
+    and, per GEMM, the first rows of `oracle_sample_rows`, extrapolated
     linearly to all M rows.  Returns (seconds per full step, description)."""
     import numpy as np
 
@@ -649,10 +711,11 @@ def oracle_step_sample(wl, gemm_budget_s):
     total = 0.0
     parts = []
     acts, ws = workload_inputs(wl)
-    rate = 2e10  # FLOP/s guess for sizing the first GEMM sample; refined as we go
+    rows_of = iter(oracle_sample_rows(wl))
     for lin in wl.linears:
         a, w = acts[lin.K], ws[lin.name]
         for mode in wl.modes:
+            rows = next(rows_of)
             if mode == "per_tensor_static":
                 s_held = oracle.scale_from_history(np.float32([oracle.amax(a, wl.in_dtype)]), 0)
                 hist = np.zeros(HIST_LEN, np.float32)
@@ -671,8 +734,6 @@ def oracle_step_sample(wl, gemm_budget_s):
                 qa, sa = oracle.quantize_per_tensor(a, wl.in_dtype)
                 qw, sw = oracle.quantize_per_tensor(w, wl.in_dtype)
             tq = time.perf_counter() - t
-            per_row = 2 * lin.N * lin.K
-            rows = int(max(1, min(lin.M, gemm_budget_s * rate / per_row)))
             t = time.perf_counter()
             if mode == "block":
                 oracle.gemm_block(qa, sa, qw, sw, rows=np.arange(rows))
@@ -685,47 +746,55 @@ def oracle_step_sample(wl, gemm_budget_s):
                 t = time.perf_counter()
                 oracle.scale_from_history(hist, HIST_MARGIN)
                 tq += time.perf_counter() - t
-            rate = rows * per_row / max(tg, 1e-9)
             total += tq + tg * lin.M / rows
             parts.append(f"{lin.name}/{mode}: quantize full, GEMM {rows}/{lin.M} rows")
     return total, "; ".join(parts)
 
 
-def cpu_baseline(wl, budget_s):
+def oracle_timing(wl, warmup, samples):
+    """`warmup` untimed sampled steps, then the median of `samples` timed
+    ones: (seconds per full step, description, thread count)."""
     import oracle
-    flops = sum(2 * lin.M * lin.N * lin.K for lin in wl.linears) * len(wl.modes)
-    nlin = len(wl.linears) * len(wl.modes)
-    t, desc = oracle_step_sample(wl, gemm_budget_s=budget_s / nlin)
-    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.get_threads(), "kind": "oracle",
-            "sample": desc + " (GEMM time extrapolated to all rows)", "s_per_step": round(t, 4)}
+    for _ in range(warmup):
+        oracle_step_sample(wl)
+    times, desc = [], ""
+    for _ in range(samples):
+        t, desc = oracle_step_sample(wl)
+        times.append(t)
+    return statistics.median(times), desc, oracle.get_threads()
+
+
+def step_flops(wl):
+    return sum(2 * lin.M * lin.N * lin.K for lin in wl.linears) * len(wl.modes)
+
+
+def baseline_entry(wl, seconds, desc, cores, warmup, samples):
+    return {"value": round(step_flops(wl) / seconds / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{desc} (GEMM time extrapolated to all rows); median of {samples} sampled steps after "
+                      f"{warmup} untimed",
+            "s_per_step": round(seconds, 4), "samples": samples}
+
+
+def cpu_baseline(wl, warmup=1, samples=3):
+    t, desc, cores = oracle_timing(wl, warmup, samples)
+    return baseline_entry(wl, t, desc, cores, warmup, samples)
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import oracle
     wl = workload_of(args)
-    flops = sum(2 * lin.M * lin.N * lin.K for lin in wl.linears) * len(wl.modes)
-    nlin = len(wl.linears) * len(wl.modes)
-    budget = 1.0 / nlin
-    for _ in range(args.warmup):
-        oracle_step_sample(wl, budget)
-    times = []
-    desc = ""
-    for _ in range(args.steps):
-        t, desc = oracle_step_sample(wl, budget)
-        times.append(t)
-    s = sum(times) / len(times)
-    value = flops / s / 1e12
+    t, desc, cores = oracle_timing(wl, args.warmup, args.steps)
+    base = baseline_entry(wl, t, desc, cores, args.warmup, args.steps)
+    value = base["value"]
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": args.workload, "description": wl.description, "modes": list(wl.modes)},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.get_threads(), "kind": "oracle",
-                         "sample": desc + " (GEMM time extrapolated to all rows)"},
-        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": config_of(args, wl),
+        "cpu_baseline": base,
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 

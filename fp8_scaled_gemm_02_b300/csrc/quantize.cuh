@@ -18,7 +18,10 @@
 //  * the E4M3 byte of fl32(x / s) is obtained without a per-element divide.
 //    Once per unit: y = RN(1/s), and ylo = RN(r*y) with the residual
 //    r = 1 - s*y (exact through an FMA), so that y + ylo is 1/s to about
-//    2^-47 (a double-word reciprocal).  Per element: q = RN(x*y + RN(x*ylo))
+//    2^-47 (a double-word reciprocal: the FMA residual correction of
+//    P. Markstein, "Computation of elementary functions on the IBM RISC
+//    System/6000 processor", IBM J. Res. Dev. 34(1), 1990; see also Muller
+//    et al., "Handbook of Floating-Point Arithmetic", division with an FMA).  Per element: q = RN(x*y + RN(x*ylo))
 //    (a multiply and an FMA, two elements at a time with the packed .f32x2
 //    instructions).  q can differ from fl32(x/s) in the last place, but
 //    never across an E4M3 rounding boundary: for every pair of FP16 or BF16

@@ -138,6 +138,9 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("llama2_7b_m128",
                  "Llama-2-7B-shaped linears at M=128 (decode batch), BF16, block-scaled, BF16 out",
                  BF16, BF16, ("block",), _llama2(128), seed=4),
+        *[Workload(f"llama2_7b_m{m}",
+                   f"Llama-2-7B-shaped linears at M={m} (decode, batch size {m}), BF16, block-scaled, BF16 out",
+                   BF16, BF16, ("block",), _llama2(m), seed=4) for m in (1, 2, 4, 8, 16)],
         Workload("llama2_7b_m4096",
                  "Llama-2-7B-shaped linears at M=4096 (prefill), BF16, block-scaled, BF16 out",
                  BF16, BF16, ("block",), _llama2(4096), seed=4),

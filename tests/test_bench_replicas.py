@@ -113,3 +113,54 @@ def test_per_channel_mode_plan():
         assert [k[0] for k in ks] == ["quant_per_tensor_act", "quant_per_channel_weight", "gemm_per_channel"]
         assert ks[1][2] == lin.N * lin.K * 3 + 4 * lin.N
         assert ks[2][2] == lin.M * lin.K + lin.N * lin.K + 4 + 4 * lin.N + 2 * lin.M * lin.N
+
+
+def test_both_arms_print_the_same_config():
+    """The GPU arm and the reference arm build `config` with one helper, so
+    the two lines name the same workload in the same words."""
+    import bench
+
+    class Args:
+        workload = bench.DEFAULT_WORKLOAD
+        modes = ""
+        gpus = 1
+
+    wl = bench.workload_of(Args())
+    cfg = bench.config_of(Args(), wl)
+    assert cfg["workload"] == "outlier_16384x8192x8192"
+    assert cfg["linears"] == [["gemm", 16384, 8192, 8192]]
+    assert set(cfg) == {"workload", "description", "linears", "modes", "in_dtype", "out_dtype", "l2", "parallelism"}
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """On rank 0 the reference arm prints one line with the shared config,
+    a cpu_baseline describing its own sample and an e2e of zero copies."""
+    import json
+
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+
+    class Args:
+        workload = "per_tensor_64x64x128"
+        modes = ""
+        gpus = 1
+        steps = 2
+        warmup = 1
+
+    bench.run_reference(Args())
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.config_of(Args(), bench.workload_of(Args()))
+    assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["samples"] == 2
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_oracle_sample_is_fixed():
+    """Both arms time the same sample: the GEMM rows depend on the workload only."""
+    import bench
+    import synth
+    wl = synth.WORKLOADS["outlier_16384x8192x8192"]
+    assert bench.oracle_sample_rows(wl) == bench.oracle_sample_rows(wl) == [149]
+    wl = synth.WORKLOADS["llama2_7b_m1"]
+    assert bench.oracle_sample_rows(wl) == [1, 1, 1, 1]
