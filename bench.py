@@ -63,6 +63,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 HIST_LEN = 16        # amax-history ring of the delayed-scaling mode
 HIST_MARGIN = 0      # the recipe's margin (DelayedScaling(margin=0, interval=4))
+MODES = ("block", "per_tensor", "per_tensor_static", "per_channel", "block_ue8m0", "fused")
+# A plain run prints one line per entry, the headline (the largest workload,
+# block-scaled with FP32 scales) last: a decode batch of one token through
+# the unfused and the fused linear, and the headline shape with power-of-two
+# (UE8M0) scales on the tensor core's block-scaled MMA.
+DEFAULT_LINES = (("llama2_7b_m1", "block,fused"), (DEFAULT_WORKLOAD, "block_ue8m0"), (DEFAULT_WORKLOAD, ""))
 
 
 def parse_args():
@@ -71,13 +77,14 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--workload", default=None,
+                   help="one workload (default: the decode and UE8M0 lines, then the headline workload)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped to ~2 s")
     p.add_argument("--modes", default="",
                    help="override the workload's scaling modes: block, per_tensor, per_channel, "
-                        "per_tensor_static (comma list)")
+                        "per_tensor_static, block_ue8m0, fused (comma list)")
     p.add_argument("--profile", type=int, default=0,
                    help="run N eager steps on one input set and exit (a small command for ncu captures)")
     a = p.parse_args()
@@ -116,7 +123,7 @@ def workload_of(args):
     wl = synth.WORKLOADS[args.workload]
     if args.modes:
         modes = tuple(args.modes.split(","))
-        bad = [m for m in modes if m not in ("block", "per_tensor", "per_tensor_static", "per_channel")]
+        bad = [m for m in modes if m not in MODES]
         if bad:
             raise SystemExit(f"unknown scaling mode(s) {bad}")
         wl = dataclasses.replace(wl, modes=modes)
@@ -140,7 +147,16 @@ def kernel_plan(wl):
     for lin in wl.linears:
         M, N, K = lin.M, lin.N, lin.K
         for mode in wl.modes:
-            if mode == "block":
+            nb, kbn = (N + 127) // 128, K // 128
+            if mode == "block_ue8m0":
+                ks = [("quant_token_group_ue8m0", "hbm", M * K * 3 + M * kbn, 0),
+                      ("quant_weight_block_ue8m0", "hbm", N * K * 3 + nb * kbn, 0),
+                      ("gemm_block_ue8m0", None, M * K + N * K + M * kbn + nb * kbn + 2 * M * N, 2 * M * N * K)]
+            elif mode == "fused":
+                # the activation is read once in 16 bits and quantized inside the GEMM
+                ks = [("quant_weight_block", "hbm", N * K * 3 + 4 * nb * kbn, 0),
+                      ("linear_fused", None, M * K * 2 + N * K + 4 * nb * kbn + 2 * M * N, 2 * M * N * K)]
+            elif mode == "block":
                 ks = [("quant_token_group", "hbm", M * K * 3 + 4 * M * (K // 128), 0),
                       ("quant_weight_block", "hbm", N * K * 3 + 4 * ((N + 127) // 128) * (K // 128), 0),
                       ("gemm_block", None, M * K + N * K + 4 * M * (K // 128) + 4 * ((N + 127) // 128) * (K // 128)
@@ -310,7 +326,7 @@ def run_ours(args):
         raise SystemExit("bench.py needs a CUDA device")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
+    if world > 1 and not dist.is_initialized():
         dist.init_process_group("nccl", device_id=dev)
 
     wl = workload_of(args)
@@ -351,9 +367,12 @@ def run_ours(args):
             b = {"qa": torch.empty((M, K), dtype=torch.uint8, device=dev),
                  "qw": torch.empty((N, K), dtype=torch.uint8, device=dev),
                  "c": torch.empty((M, N), dtype=out_t, device=dev)}
-            if mode == "block":
+            if mode in ("block", "fused"):
                 b["sa"] = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
                 b["sw"] = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
+            elif mode == "block_ue8m0":
+                b["sa"] = torch.empty((K // 128, M), dtype=torch.uint8, device=dev)
+                b["sw"] = torch.empty(((N + 127) // 128, K // 128), dtype=torch.uint8, device=dev)
             else:
                 b["sa"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
                 b["sw"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
@@ -376,7 +395,16 @@ def run_ours(args):
             a = s["a"][lin.K]
             w = s["w"][lin.name]
             post = []
-            if mode == "block":
+            if mode == "fused":
+                ca = None
+                cw = lambda w=w, b=b: F.fp8_quantize_weight_block(w, q=b["qw"], sb=b["sw"])
+                cg = lambda a=a, b=b: F.fp8_linear_token_group(a, b["qw"], b["sw"], c=b["c"])
+            elif mode == "block_ue8m0":
+                ca = lambda a=a, b=b: F.fp8_quantize_token_group_ue8m0(a, q=b["qa"], sa=b["sa"])
+                cw = lambda w=w, b=b: F.fp8_quantize_weight_block_ue8m0(w, q=b["qw"], sb=b["sw"])
+                cg = lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
+                                                   mode="block_ue8m0", c=b["c"])
+            elif mode == "block":
                 ca = lambda a=a, b=b: F.fp8_quantize_token_group(a, q=b["qa"], sa=b["sa"])
                 cw = lambda w=w, b=b: F.fp8_quantize_weight_block(w, q=b["qw"], sb=b["sw"])
                 cg = lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
@@ -403,7 +431,7 @@ def run_ours(args):
     def kernel_calls(r):
         """The step's kernels for rotation set r, as zero-argument callables
         (the order of the kernels in `plan`)."""
-        return [c for ca, cw, cg, post in linear_calls(r) for c in (ca, cw, cg, *post)]
+        return [c for ca, cw, cg, post in linear_calls(r) for c in (ca, cw, cg, *post) if c is not None]
 
     side = torch.cuda.Stream(device=dev)
 
@@ -413,6 +441,12 @@ def run_ours(args):
         are independent), then the GEMM runs on `main` after both, followed
         by the linear's post-GEMM calls (the delayed-scaling update)."""
         for ca, cw, cg, post in linear_calls(r):
+            if ca is None:   # fused: the GEMM quantizes the activation itself
+                cw()
+                cg()
+                for c in post:
+                    c()
+                continue
             ev_fork = torch.cuda.Event()
             ev_fork.record(main)
             side.wait_event(ev_fork)
@@ -665,8 +699,6 @@ def run_ours(args):
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
 
 
 # ----------------------------------------------------------- CPU oracle arm
@@ -720,9 +752,13 @@ def oracle_step_sample(wl):
                 s_held = oracle.scale_from_history(np.float32([oracle.amax(a, wl.in_dtype)]), 0)
                 hist = np.zeros(HIST_LEN, np.float32)
             t = time.perf_counter()
-            if mode == "block":
+            if mode in ("block", "fused"):
                 qa, sa = oracle.quantize_token_group(a, wl.in_dtype)
                 qw, sw = oracle.quantize_weight_block(w, wl.in_dtype)
+            elif mode == "block_ue8m0":
+                qa, ca = oracle.quantize_token_group_ue8m0(a, wl.in_dtype)
+                qw, cw = oracle.quantize_weight_block_ue8m0(w, wl.in_dtype)
+                sa, sw = oracle.ue8m0_decode(ca), oracle.ue8m0_decode(cw)
             elif mode == "per_channel":
                 qa, sa = oracle.quantize_per_tensor(a, wl.in_dtype)
                 qw, sw = oracle.quantize_per_channel(w, wl.in_dtype)
@@ -735,7 +771,7 @@ def oracle_step_sample(wl):
                 qw, sw = oracle.quantize_per_tensor(w, wl.in_dtype)
             tq = time.perf_counter() - t
             t = time.perf_counter()
-            if mode == "block":
+            if mode in ("block", "fused", "block_ue8m0"):
                 oracle.gemm_block(qa, sa, qw, sw, rows=np.arange(rows))
             elif mode == "per_channel":
                 oracle.gemm_per_channel(qa, sa, qw, sw, rows=np.arange(rows))
@@ -799,12 +835,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def lines_of(args):
+    """(workload, modes) of every line to print: the one asked for, or the
+    default set with the headline workload last."""
+    import copy
+    todo = [(args.workload, args.modes)] if args.workload else list(DEFAULT_LINES)
+    out = []
+    for wl, modes in todo:
+        a = copy.copy(args)
+        a.workload, a.modes = wl, modes
+        out.append(a)
+    return out
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
-        run_reference(args)
-    else:
-        run_ours(args)
+    for a in lines_of(args):
+        if args.impl == "reference":
+            run_reference(a)
+        else:
+            run_ours(a)
+            import gc
+
+            import torch
+            gc.collect()
+            torch.cuda.empty_cache()
+    if args.impl != "reference" and dist_env()[1] > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":

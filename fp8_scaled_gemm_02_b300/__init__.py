@@ -12,6 +12,11 @@ only marshal torch tensors (device memory, current stream) into them:
   fp8_quantize_weight_block(w [N,K])    -> (q, sb [N/128,K/128]) 128x128 blocks
   fp8_quantize_per_channel(w [N,K])     -> (q, sb [N])       one scale per output channel
   fp8_gemm_scaled(qa, sa, qb, sb, ...)  -> C [M,N] FP16/BF16
+  fp8_quantize_token_group_ue8m0(x)     -> (q, sa_code uint8 [K/128,M])   power-of-two scales
+  fp8_quantize_weight_block_ue8m0(w)    -> (q, sb_code uint8 [N/128,K/128])
+  fp8_linear_token_group(x, qw, sw)     -> C [M,N]         fused: x quantized inside the GEMM
+  fp8_e5m2_encode(x) / fp8_e5m2_decode(q, dtype)
+                                        E5M2 codec (5 exponent + 2 mantissa bits)
 
 The path is the FP8 linear layer of "What is FP8 inference on H100
 (Transformer Engine)?" s3 (amax -> scale = amax/448 -> x/scale rounded to
@@ -23,21 +28,24 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (FP8S_BF16, FP8S_F16, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_CHANNEL, FP8S_SCALE_PER_TENSOR,
-                   Fp8sError, check, load, status_string)
+from ._lib import (FP8S_BF16, FP8S_F16, FP8S_SCALE_BLOCK, FP8S_SCALE_BLOCK_UE8M0, FP8S_SCALE_PER_CHANNEL,
+                   FP8S_SCALE_PER_TENSOR, Fp8sError, check, load, status_string)
 
 __all__ = [
     "fp8_quantize_per_tensor", "fp8_quantize_per_tensor_static", "fp8_scale_from_amax_history",
     "fp8_quantize_token_group", "fp8_quantize_per_channel", "fp8_quantize_weight_block", "fp8_gemm_scaled",
-    "fp8s_device_error", "fp8s_version", "fp8s_gemm_override", "fp8s_gemm_plan", "Fp8sError", "status_string", "load", "LIB_PATH",
+    "fp8_e5m2_encode", "fp8_e5m2_decode", "fp8_linear_token_group", "fp8_quantize_token_group_ue8m0", "fp8_quantize_weight_block_ue8m0",
+    "fp8s_device_error", "fp8s_version", "fp8s_set_exchange_timeout_ns", "fp8s_gemm_override", "fp8s_gemm_plan", "Fp8sError", "status_string", "load", "LIB_PATH",
     "FP8S_F16", "FP8S_BF16", "FP8S_SCALE_PER_TENSOR", "FP8S_SCALE_BLOCK", "FP8S_SCALE_PER_CHANNEL",
+    "FP8S_SCALE_BLOCK_UE8M0",
 ]
 
 LIB_PATH = _lib.LIB_PATH
 load()  # fail at import time if the CUDA library is missing
 
 _DT = {torch.float16: FP8S_F16, torch.bfloat16: FP8S_BF16}
-_MODE = {"per_tensor": FP8S_SCALE_PER_TENSOR, "block": FP8S_SCALE_BLOCK, "per_channel": FP8S_SCALE_PER_CHANNEL}
+_MODE = {"per_tensor": FP8S_SCALE_PER_TENSOR, "block": FP8S_SCALE_BLOCK, "per_channel": FP8S_SCALE_PER_CHANNEL,
+         "block_ue8m0": FP8S_SCALE_BLOCK_UE8M0}
 
 
 def _stream(stream):
@@ -66,6 +74,13 @@ def _need_f32(*ts):
     for t in ts:
         if t is not None and t.dtype != torch.float32:
             raise TypeError(f"scale / amax / history tensors must be float32, got {t.dtype}")
+
+
+def _need_u8(*ts):
+    """Byte outputs (E4M3 / E5M2 codes, UE8M0 scale codes)."""
+    for t in ts:
+        if t.dtype != torch.uint8 or not (t.is_cuda and t.is_contiguous()):
+            raise TypeError(f"byte outputs must be contiguous uint8 CUDA tensors, got {t.dtype}")
 
 
 def fp8_quantize_per_tensor(x, q=None, scale=None, stream=None):
@@ -143,7 +158,8 @@ def fp8_quantize_per_channel(w, q=None, sb=None, stream=None):
 def fp8_gemm_scaled(qa, sa, qb, sb, out_dtype=torch.bfloat16, mode="block", c=None, stream=None):
     """qa [M,K] uint8, qb [N,K] uint8 -> C [M,N] (FP16/BF16) = rescaled qa.qb^T.
     mode: "per_tensor" (sa, sb one float each), "block" (sa [K/128,M], sb
-    [N/128,K/128]) or "per_channel" (sa one float, sb [N])."""
+    [N/128,K/128]), "per_channel" (sa one float, sb [N]) or "block_ue8m0"
+    (the block layout with uint8 UE8M0 codes, applied by the tensor core)."""
     _need_cuda(qa, sa, qb, sb)
     M, K = qa.shape
     N = qb.shape[0]
@@ -154,6 +170,73 @@ def fp8_gemm_scaled(qa, sa, qb, sb, out_dtype=torch.bfloat16, mode="block", c=No
                                 _MODE[mode], _stream(stream))
     check(st, "fp8_gemm_scaled")
     return c
+
+
+def fp8_linear_token_group(x, qw, sw, c=None, qa=None, sa=None, stream=None):
+    """Fused FP8 linear: x [M,K] FP16/BF16 (quantized per 1x128 token group
+    inside the GEMM), qw [N,K] uint8 and sw [N/128,K/128] float32 from
+    fp8_quantize_weight_block -> C [M,N] in x's dtype.  qa/sa (uint8 [M,K],
+    float32 [K/128,M]) optionally receive the quantized activation."""
+    _need_cuda(x, qw, sw)
+    M, K = x.shape
+    N = qw.shape[0]
+    c = torch.empty((M, N), dtype=x.dtype, device=x.device) if c is None else c
+    _need_cuda(c)
+    if c.dtype != x.dtype:
+        raise TypeError("the fused linear writes C in the activation's dtype")
+    _need_f32(sw, sa)
+    st = load().fp8_linear_token_group(_ptr(x), _in_dtype(x), M, K, _ptr(qw), _ptr(sw), N, _ptr(c),
+                                       None if qa is None else _ptr(qa), None if sa is None else _ptr(sa),
+                                       _stream(stream))
+    check(st, "fp8_linear_token_group")
+    return c
+
+
+def fp8_quantize_token_group_ue8m0(x, q=None, sa=None, stream=None):
+    """x [M,K] FP16/BF16 -> (q uint8 [M,K], sa uint8 [K/128, M] UE8M0 codes)."""
+    _need_cuda(x)
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+    sa = torch.empty((K // 128, M), dtype=torch.uint8, device=x.device) if sa is None else sa
+    _need_u8(q, sa)
+    st = load().fp8_quantize_token_group_ue8m0(_ptr(x), _in_dtype(x), M, K, _ptr(q), _ptr(sa), _stream(stream))
+    check(st, "fp8_quantize_token_group_ue8m0")
+    return q, sa
+
+
+def fp8_quantize_weight_block_ue8m0(w, q=None, sb=None, stream=None):
+    """w [N,K] FP16/BF16 -> (q uint8 [N,K], sb uint8 [ceil(N/128), K/128] UE8M0 codes)."""
+    _need_cuda(w)
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
+    sb = torch.empty(((N + 127) // 128, K // 128), dtype=torch.uint8, device=w.device) if sb is None else sb
+    _need_u8(q, sb)
+    st = load().fp8_quantize_weight_block_ue8m0(_ptr(w), _in_dtype(w), N, K, _ptr(q), _ptr(sb), _stream(stream))
+    check(st, "fp8_quantize_weight_block_ue8m0")
+    return q, sb
+
+
+def fp8_e5m2_encode(x, q=None, stream=None):
+    """x (any shape, FP16/BF16) -> q uint8 same shape: E5M2 bytes, round to
+    nearest even, saturating at +-57344."""
+    _need_cuda(x)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if q is None else q
+    _need_cuda(q)
+    st = load().fp8_e5m2_encode(_ptr(x), _in_dtype(x), x.numel(), _ptr(q), _stream(stream))
+    check(st, "fp8_e5m2_encode")
+    return q
+
+
+def fp8_e5m2_decode(q, out_dtype=torch.float16, y=None, stream=None):
+    """q uint8 E5M2 bytes (any shape) -> y FP16/BF16 same shape (exact)."""
+    _need_cuda(q)
+    if out_dtype not in _DT:
+        raise TypeError("out_dtype must be float16 or bfloat16")
+    y = torch.empty(q.shape, dtype=out_dtype, device=q.device) if y is None else y
+    _need_cuda(y)
+    st = load().fp8_e5m2_decode(_ptr(q), q.numel(), _ptr(y), _DT[y.dtype], _stream(stream))
+    check(st, "fp8_e5m2_decode")
+    return y
 
 
 def fp8s_device_error(stream=None):
@@ -176,6 +259,12 @@ def fp8s_gemm_plan(M, N, K, mode="block", sms=148):
     check(load().fp8s_gemm_plan(int(M), int(N), int(K), _MODE[mode], int(sms), ctypes.byref(bn), ctypes.byref(sp),
                                 ctypes.byref(pr)), "fp8s_gemm_plan")
     return bn.value, sp.value, bool(pr.value)
+
+
+def fp8s_set_exchange_timeout_ns(ns=0):
+    """Test aid: the per-tensor quantizer's exchange-spin limit for inputs
+    above ~29 MB (0 = the default 2 s)."""
+    check(load().fp8s_set_exchange_timeout_ns(int(ns)), "fp8s_set_exchange_timeout_ns")
 
 
 def fp8s_version():

@@ -17,7 +17,7 @@ STATUS_NAMES = {
     5: "FP8S_ERR_CUDA", 6: "FP8S_ERR_DEVICE_TIMEOUT", 7: "FP8S_ERR_UNSUPPORTED_DEVICE",
 }
 FP8S_F16, FP8S_BF16 = 0, 1
-FP8S_SCALE_PER_TENSOR, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_CHANNEL = 0, 1, 2
+FP8S_SCALE_PER_TENSOR, FP8S_SCALE_BLOCK, FP8S_SCALE_PER_CHANNEL, FP8S_SCALE_BLOCK_UE8M0 = 0, 1, 2, 3
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -32,10 +32,16 @@ SIGNATURES = {
     "fp8_quantize_weight_block": (_I, [_P, _I, _I64, _I64, _P, _P, _P]),
     "fp8_quantize_per_channel": (_I, [_P, _I, _I64, _I64, _P, _P, _P]),
     "fp8_gemm_scaled": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P]),
+    "fp8_quantize_token_group_ue8m0": (_I, [_P, _I, _I64, _I64, _P, _P, _P]),
+    "fp8_quantize_weight_block_ue8m0": (_I, [_P, _I, _I64, _I64, _P, _P, _P]),
+    "fp8_linear_token_group": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _P, _P, _P, _P]),
+    "fp8_e5m2_encode": (_I, [_P, _I, _I64, _P, _P]),
+    "fp8_e5m2_decode": (_I, [_P, _I64, _P, _I, _P]),
     "fp8s_status_string": (ctypes.c_char_p, [_I]),
     "fp8s_last_cuda_error": (ctypes.c_char_p, []),
     "fp8s_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "fp8s_version": (_I, []),
+    "fp8s_set_exchange_timeout_ns": (_I, [ctypes.c_ulonglong]),
     "fp8s_gemm_override": (_I, [_I, _I, _I]),
     "fp8s_gemm_plan": (_I, [_I64, _I64, _I64, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
 }

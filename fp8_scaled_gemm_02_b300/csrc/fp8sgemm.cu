@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -16,6 +17,7 @@
 #include <unordered_map>
 
 #include "../../include/fp8sgemm.h"
+#include "codec.cuh"
 #include "gemm.cuh"
 #include "quantize.cuh"
 
@@ -24,6 +26,10 @@ namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per mbarrier wait
+// Limit of the per-tensor quantizer's grid-wide exchange spin when it
+// streams its slices (no bulk copy in flight): the default, or the value a
+// test set with fp8s_set_exchange_timeout_ns to make the spin run out.
+std::atomic<unsigned long long> g_exchange_timeout_ns{kWaitTimeoutNs};
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -207,11 +213,11 @@ fp8s_status ensure_smem_attr(KernelT kern, int bytes, bool* done_per_device) {
 }
 
 // ------------------------------------------------------------ quantizers
-template <int DT, int GPW>
-fp8s_status launch_token_group_gpw(const void* x, int64_t M, int64_t G, uint8_t* q, float* sa, cudaStream_t st,
+template <int DT, int GPW, bool UE8>
+fp8s_status launch_token_group_gpw(const void* x, int64_t M, int64_t G, uint8_t* q, void* sa, cudaStream_t st,
                                    const DeviceInfo& info) {
   static bool attr_done[kMaxDevices] = {};
-  auto kern = quant_token_group_kernel<DT, GPW>;
+  auto kern = quant_token_group_kernel<DT, GPW, UE8>;
   constexpr int kSmem = tg_smem_bytes(GPW);
   if (fp8s_status s = ensure_smem_attr(kern, kSmem, attr_done)) return s;
   const int64_t groups = M * G;
@@ -223,25 +229,26 @@ fp8s_status launch_token_group_gpw(const void* x, int64_t M, int64_t G, uint8_t*
 }
 
 // Groups per consumer warp: the largest that still gives every SM two chunks.
-template <int DT>
-fp8s_status launch_token_group(const void* x, int64_t M, int64_t K, uint8_t* q, float* sa, cudaStream_t st,
+// `sa` receives FP32 scales, or UE8M0 codes when UE8.
+template <int DT, bool UE8 = false>
+fp8s_status launch_token_group(const void* x, int64_t M, int64_t K, uint8_t* q, void* sa, cudaStream_t st,
                                const DeviceInfo& info) {
   const int64_t G = K / 128;
   const int64_t groups = M * G;
   const int64_t want = 2LL * info.sms;
-  if (groups >= want * 8 * 16) return launch_token_group_gpw<DT, 16>(x, M, G, q, sa, st, info);
-  if (groups >= want * 8 * 8) return launch_token_group_gpw<DT, 8>(x, M, G, q, sa, st, info);
-  if (groups >= want * 8 * 4) return launch_token_group_gpw<DT, 4>(x, M, G, q, sa, st, info);
-  return launch_token_group_gpw<DT, 2>(x, M, G, q, sa, st, info);
+  if (groups >= want * 8 * 16) return launch_token_group_gpw<DT, 16, UE8>(x, M, G, q, sa, st, info);
+  if (groups >= want * 8 * 8) return launch_token_group_gpw<DT, 8, UE8>(x, M, G, q, sa, st, info);
+  if (groups >= want * 8 * 4) return launch_token_group_gpw<DT, 4, UE8>(x, M, G, q, sa, st, info);
+  return launch_token_group_gpw<DT, 2, UE8>(x, M, G, q, sa, st, info);
 }
 
-template <int DT>
-fp8s_status launch_weight_block(const void* w, int64_t N, int64_t K, uint8_t* q, float* sb, cudaStream_t st,
+template <int DT, bool UE8 = false>
+fp8s_status launch_weight_block(const void* w, int64_t N, int64_t K, uint8_t* q, void* sb, cudaStream_t st,
                                 const DeviceInfo& info, int dev) {
   CUtensorMap mw;
   if (fp8s_status s = tensor_map_2d(w, N, K, 2, 128, 128, false, dev, &mw)) return s;
   static bool attr_done[kMaxDevices] = {};
-  auto kern = quant_weight_block_tma_kernel<DT>;
+  auto kern = quant_weight_block_tma_kernel<DT, UE8>;
   if (fp8s_status s = ensure_smem_attr(kern, kWbSmemBytes, attr_done)) return s;
   const int64_t nblocks = ((N + 127) / 128) * (K / 128);
   const int64_t cap = info.sms;  // one CTA per SM
@@ -350,9 +357,11 @@ fp8s_status launch_per_tensor(const void* x, int64_t numel, uint8_t* q, float* s
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Streamed slices: the kernel's only waits are the exchange spins.
+  const unsigned long long tmo = resident ? kWaitTimeoutNs : g_exchange_timeout_ns.load();
   if (const cudaError_t e =
           cudaLaunchKernelEx(&cfg, kern, static_cast<const uint4*>(x), nvec, tail, ntail, reinterpret_cast<uint2*>(q),
-                             q + nvec * 8, word, resident ? 1 : 0, kWaitTimeoutNs);
+                             q + nvec * 8, word, resident ? 1 : 0, tmo);
       e != cudaSuccess)
     return cuda_fail(e);
   return FP8S_OK;
@@ -426,6 +435,32 @@ fp8s_status launch_per_channel(const void* w, int64_t N, int64_t K, uint8_t* q, 
                    reinterpret_cast<uint2*>(q), sb);
 }
 
+// ---------------------------------------------------------------- E5M2
+// One wave of 256-thread CTAs (8 per SM), fewer for small inputs.
+unsigned codec_grid(int64_t units, const DeviceInfo& info) {
+  const int64_t want = (units + kCodecThreads - 1) / kCodecThreads;
+  const int64_t cap = 8LL * info.sms;
+  return static_cast<unsigned>(std::max<int64_t>(1, std::min(want, cap)));
+}
+
+template <int DT>
+fp8s_status launch_e5m2_encode(const void* x, int64_t numel, uint8_t* q, cudaStream_t st, const DeviceInfo& info) {
+  const int64_t nvec = numel / 8;
+  const int ntail = static_cast<int>(numel - nvec * 8);
+  return launch_ex(e5m2_encode_kernel<DT>, codec_grid(nvec, info), kCodecThreads, 0, st, 1,
+                   static_cast<const uint4*>(x), nvec, static_cast<const uint16_t*>(x) + nvec * 8, ntail,
+                   reinterpret_cast<uint2*>(q), q + nvec * 8);
+}
+
+template <int DT>
+fp8s_status launch_e5m2_decode(const uint8_t* q, int64_t numel, void* y, cudaStream_t st, const DeviceInfo& info) {
+  const int64_t nvec = numel / 16;
+  const int ntail = static_cast<int>(numel - nvec * 16);
+  return launch_ex(e5m2_decode_kernel<DT>, codec_grid(nvec, info), kCodecThreads, 0, st, 1,
+                   reinterpret_cast<const uint4*>(q), nvec, q + nvec * 16, ntail, static_cast<uint4*>(y),
+                   static_cast<uint16_t*>(y) + nvec * 16);
+}
+
 // ------------------------------------------------------------------ GEMM
 struct GemmChoice {
   int bn = 128;
@@ -474,11 +509,11 @@ int max_active_clusters(KernelT kern, int threads, int smem, int splits, int dev
   return n;
 }
 
-template <int BN, int MODE, int OUT, bool SPLIT, bool PAIR>
+template <int BN, int MODE, int OUT, bool SPLIT, bool PAIR, int FR = 0>
 fp8s_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int splits,
                             const DeviceInfo& info, int dev, cudaStream_t st) {
-  using Cfg = GemmCfg<BN, MODE, SPLIT, PAIR>;
-  auto kern = fp8_gemm_kernel<BN, MODE, OUT, SPLIT, PAIR>;
+  using Cfg = GemmCfg<BN, MODE, SPLIT, PAIR, FR>;
+  auto kern = fp8_gemm_kernel<BN, MODE, OUT, SPLIT, PAIR, FR>;
   static bool attr_set[kMaxDevices] = {};
   if (fp8s_status s = ensure_smem_attr(kern, Cfg::kSmemBytes, attr_set)) return s;
   if constexpr (PAIR) {
@@ -537,12 +572,13 @@ double estimate_us(int64_t M, int64_t N, int64_t KB, int mode, int sms, int bn, 
   return t + 2.5 + (s > 1 ? 4.0 : 0.0) + (pair ? 0.7 : 0.0);  // a pair also waits on a cluster barrier to start
 }
 
-GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms) {
+GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms, int max_bn = 256, int min_bn = 32) {
   GemmChoice best;
   double best_t = 1e300;
   const int bns[] = {256, 192, 128, 64, 32};
   const int64_t tm = (M + kBM - 1) / kBM;
   for (int bn : bns) {
+    if (bn > max_bn || bn < min_bn) continue;
     for (int s = 1; s <= 8; s *= 2) {
       if (s > KB || (s > 1 && bn > 192)) continue;
       const int64_t tiles = tm * ((N + bn - 1) / bn);
@@ -552,7 +588,7 @@ GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms) {
         const bool pair = pr != 0;
         // pairs pay off from M = 1024 up (at M = 512, per-tensor 512x11264x2048:
         // 19.8 us paired vs 17.7 us single-CTA 128x192 tiles)
-        if (pair && (s > 1 || bn < 64 || M < 1024)) continue;
+        if (pair && (s > 1 || bn < 64 || M < 1024 || mode == FP8S_SCALE_BLOCK_UE8M0)) continue;
         const double t = estimate_us(M, N, KB, mode, sms, bn, s, pair);
         if (t < best_t * 0.999) {
           best_t = t;
@@ -570,12 +606,16 @@ template <int MODE, int OUT>
 fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                           const DeviceInfo& info, int dev, cudaStream_t st) {
   if (ch.pair) {
-    switch (ch.bn) {
-      case 64: return launch_gemm_cfg<64, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
-      case 128: return launch_gemm_cfg<128, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
-      case 192: return launch_gemm_cfg<192, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
-      case 256: return launch_gemm_cfg<256, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
-      default: return FP8S_ERR_SHAPE;
+    if constexpr (MODE == kModeUE8) {
+      return FP8S_ERR_SHAPE;  // scale factors are staged per CTA: no CTA pairs
+    } else {
+      switch (ch.bn) {
+        case 64: return launch_gemm_cfg<64, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+        case 128: return launch_gemm_cfg<128, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+        case 192: return launch_gemm_cfg<192, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+        case 256: return launch_gemm_cfg<256, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
+        default: return FP8S_ERR_SHAPE;
+      }
     }
   }
   if (ch.splits > 1) {
@@ -593,6 +633,25 @@ fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUt
     case 128: return launch_gemm_cfg<128, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
     case 192: return launch_gemm_cfg<192, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
     case 256: return launch_gemm_cfg<256, MODE, OUT, false, false>(ma, mb, p, 1, info, dev, st);
+    default: return FP8S_ERR_SHAPE;
+  }
+}
+
+// The fused linear: block mode, single-CTA tiles of 64 or 128 columns, with
+// or without split-K; FR-row activation boxes.
+template <int OUT, int FR>
+fp8s_status dispatch_fused(const GemmChoice& ch, const CUtensorMap& mx, const CUtensorMap& mb, const GemmParams& p,
+                           const DeviceInfo& info, int dev, cudaStream_t st) {
+  if (ch.splits > 1) {
+    switch (ch.bn) {
+      case 64: return launch_gemm_cfg<64, kModeBlock, OUT, true, false, FR>(mx, mb, p, ch.splits, info, dev, st);
+      case 128: return launch_gemm_cfg<128, kModeBlock, OUT, true, false, FR>(mx, mb, p, ch.splits, info, dev, st);
+      default: return FP8S_ERR_SHAPE;
+    }
+  }
+  switch (ch.bn) {
+    case 64: return launch_gemm_cfg<64, kModeBlock, OUT, false, false, FR>(mx, mb, p, 1, info, dev, st);
+    case 128: return launch_gemm_cfg<128, kModeBlock, OUT, false, false, FR>(mx, mb, p, 1, info, dev, st);
     default: return FP8S_ERR_SHAPE;
   }
 }
@@ -674,6 +733,37 @@ fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int64_t N, i
                         : launch_weight_block<kInBF16>(w, N, K, q, sb, st, info, dev);
 }
 
+fp8s_status fp8_quantize_token_group_ue8m0(const void* x, fp8s_dtype xt, int64_t M, int64_t K, uint8_t* q,
+                                           uint8_t* sa_code, fp8s_stream_t stream) {
+  if (xt != FP8S_F16 && xt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!x || !q || !sa_code) return FP8S_ERR_NULL;
+  if (M < 1 || K < 128 || K % 128 != 0 || M > (1LL << 31) - 1 || M * (K / 128) > (1LL << 31) - 1)
+    return FP8S_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sa_code)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return xt == FP8S_F16 ? launch_token_group<kInF16, true>(x, M, K, q, sa_code, st, info)
+                        : launch_token_group<kInBF16, true>(x, M, K, q, sa_code, st, info);
+}
+
+fp8s_status fp8_quantize_weight_block_ue8m0(const void* w, fp8s_dtype wt, int64_t N, int64_t K, uint8_t* q,
+                                            uint8_t* sb_code, fp8s_stream_t stream) {
+  if (wt != FP8S_F16 && wt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!w || !q || !sb_code) return FP8S_ERR_NULL;
+  if (N < 1 || K < 128 || K % 128 != 0 || K / 128 > 65535 || N > (1LL << 31) - 128 ||
+      ((N + 127) / 128) * (K / 128) > (1LL << 31) - 1)
+    return FP8S_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(sb_code)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return wt == FP8S_F16 ? launch_weight_block<kInF16, true>(w, N, K, q, sb_code, st, info, dev)
+                        : launch_weight_block<kInBF16, true>(w, N, K, q, sb_code, st, info, dev);
+}
+
 fp8s_status fp8_quantize_per_channel(const void* w, fp8s_dtype wt, int64_t N, int64_t K, uint8_t* q, float* sb,
                                      fp8s_stream_t stream) {
   if (wt != FP8S_F16 && wt != FP8S_BF16) return FP8S_ERR_DTYPE;
@@ -688,18 +778,45 @@ fp8s_status fp8_quantize_per_channel(const void* w, fp8s_dtype wt, int64_t N, in
                         : launch_per_channel<kInBF16>(w, N, K, q, sb, st, info, dev);
 }
 
+fp8s_status fp8_e5m2_encode(const void* x, fp8s_dtype xt, int64_t numel, uint8_t* q, fp8s_stream_t stream) {
+  if (xt != FP8S_F16 && xt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!x || !q) return FP8S_ERR_NULL;
+  if (numel < 1) return FP8S_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return xt == FP8S_F16 ? launch_e5m2_encode<kInF16>(x, numel, q, st, info)
+                        : launch_e5m2_encode<kInBF16>(x, numel, q, st, info);
+}
+
+fp8s_status fp8_e5m2_decode(const uint8_t* q, int64_t numel, void* y, fp8s_dtype yt, fp8s_stream_t stream) {
+  if (yt != FP8S_F16 && yt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!q || !y) return FP8S_ERR_NULL;
+  if (numel < 1) return FP8S_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(y)) return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+  return yt == FP8S_F16 ? launch_e5m2_decode<kInF16>(q, numel, y, st, info)
+                        : launch_e5m2_decode<kInBF16>(q, numel, y, st, info);
+}
+
 fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, void* c,
                             fp8s_dtype ct, int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode_in,
                             fp8s_stream_t stream) {
   if (ct != FP8S_F16 && ct != FP8S_BF16) return FP8S_ERR_DTYPE;
-  if (mode_in != FP8S_SCALE_PER_TENSOR && mode_in != FP8S_SCALE_BLOCK && mode_in != FP8S_SCALE_PER_CHANNEL)
+  if (mode_in != FP8S_SCALE_PER_TENSOR && mode_in != FP8S_SCALE_BLOCK && mode_in != FP8S_SCALE_PER_CHANNEL &&
+      mode_in != FP8S_SCALE_BLOCK_UE8M0)
     return FP8S_ERR_DTYPE;
   // per-channel weights run the per-tensor kernels with a per-column sB
   const bool per_col = mode_in == FP8S_SCALE_PER_CHANNEL;
   const fp8s_scale_mode mode = per_col ? FP8S_SCALE_PER_TENSOR : mode_in;
   if (!qa || !sa || !qb || !sb || !c) return FP8S_ERR_NULL;
   if (M < 1 || N < 1 || K < 16 || K % 16 != 0) return FP8S_ERR_SHAPE;
-  if (mode == FP8S_SCALE_BLOCK && K % 128 != 0) return FP8S_ERR_SHAPE;
+  if ((mode == FP8S_SCALE_BLOCK || mode == FP8S_SCALE_BLOCK_UE8M0) && K % 128 != 0) return FP8S_ERR_SHAPE;
   if (M > (1LL << 31) - 256 || N > (1LL << 31) - 256 || K > (1LL << 31) - 256 || M * N > (1LL << 40))
     return FP8S_ERR_SHAPE;
   if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb) || !aligned16(c)) return FP8S_ERR_ALIGN;
@@ -715,6 +832,7 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
     ch.splits = g_force_splits > 0 ? g_force_splits : 1;
     ch.pair = g_force_pair != 0;
     if (ch.splits > KB) return FP8S_ERR_SHAPE;
+    if (ch.pair && mode == FP8S_SCALE_BLOCK_UE8M0) return FP8S_ERR_SHAPE;
   }
   const int bn = ch.bn;
   const int tile_m = ch.pair ? 2 * kBM : kBM;
@@ -722,7 +840,7 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
   if (fp8s_status s = tensor_map_e4m3(qa, M, K, kBM, dev, &ma)) return s;
   if (fp8s_status s = tensor_map_e4m3(qb, N, K, ch.pair ? bn / 2 : bn, dev, &mb)) return s;
 
-  GemmParams p;
+  GemmParams p{};
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
@@ -745,6 +863,9 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
     if (mode == FP8S_SCALE_PER_TENSOR)
       return ct == FP8S_F16 ? dispatch_gemm<kModePerTensor, kOutF16>(c, ma, mb, p, info, dev, st)
                             : dispatch_gemm<kModePerTensor, kOutBF16>(c, ma, mb, p, info, dev, st);
+    if (mode == FP8S_SCALE_BLOCK_UE8M0)
+      return ct == FP8S_F16 ? dispatch_gemm<kModeUE8, kOutF16>(c, ma, mb, p, info, dev, st)
+                            : dispatch_gemm<kModeUE8, kOutBF16>(c, ma, mb, p, info, dev, st);
     return ct == FP8S_F16 ? dispatch_gemm<kModeBlock, kOutF16>(c, ma, mb, p, info, dev, st)
                           : dispatch_gemm<kModeBlock, kOutBF16>(c, ma, mb, p, info, dev, st);
   };
@@ -757,14 +878,74 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
   return r;
 }
 
+fp8s_status fp8_linear_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K, const uint8_t* qw,
+                                   const float* sw, int64_t N, void* c, uint8_t* qa, float* sa, fp8s_stream_t stream) {
+  if (xt != FP8S_F16 && xt != FP8S_BF16) return FP8S_ERR_DTYPE;
+  if (!x || !qw || !sw || !c || (!qa) != (!sa)) return FP8S_ERR_NULL;
+  if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return FP8S_ERR_SHAPE;
+  if (M > (1LL << 31) - 256 || N > (1LL << 31) - 256 || K > (1LL << 31) - 256 || M * N > (1LL << 40) ||
+      M * (K / 128) > (1LL << 31) - 1)
+    return FP8S_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(qw) || !aligned16(sw) || !aligned16(c) || (qa && (!aligned16(qa) || !aligned16(sa))))
+    return FP8S_ERR_ALIGN;
+  int dev;
+  DeviceInfo info;
+  if (fp8s_status s = current_device(&dev, &info)) return s;
+  cudaStream_t st = as_stream(stream);
+
+  const int64_t KB = K / kBK;
+  GemmChoice ch = choose_gemm(M, N, KB, FP8S_SCALE_BLOCK, info.sms, 128, 64);  // the fused kernel's tile widths
+  if (g_force_bn) {
+    ch.bn = g_force_bn;
+    ch.splits = g_force_splits > 0 ? g_force_splits : 1;
+    if (g_force_pair || (ch.bn != 64 && ch.bn != 128) || ch.splits > KB) return FP8S_ERR_SHAPE;
+  }
+  const int fr = M <= 16 ? 16 : 128;   // rows of the activation box: M <= 16 needs only 16
+  CUtensorMap mx, mb;
+  if (fp8s_status s = tensor_map_2d(x, M, K, 2, fr, kBK, false, dev, &mx)) return s;
+  if (fp8s_status s = tensor_map_e4m3(qw, N, K, ch.bn, dev, &mb)) return s;
+
+  GemmParams p{};
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_kb = static_cast<int>(KB);
+  p.tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+  p.tiles_n = static_cast<int>((N + ch.bn - 1) / ch.bn);
+  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (tiles > (1LL << 31) - 1) return FP8S_ERR_SHAPE;
+  p.num_tiles = static_cast<int>(tiles);
+  p.group_m = p.tiles_m < 16 ? p.tiles_m : 16;
+  p.sa = nullptr;
+  p.sb = sw;
+  p.c = c;
+  p.timeout_ns = kWaitTimeoutNs;
+  p.qa_out = qa;
+  p.sa_out = sa;
+  auto run = [&](const GemmChoice& cc) {
+    if (xt == FP8S_F16)
+      return fr == 16 ? dispatch_fused<kOutF16, 16>(cc, mx, mb, p, info, dev, st)
+                      : dispatch_fused<kOutF16, 128>(cc, mx, mb, p, info, dev, st);
+    return fr == 16 ? dispatch_fused<kOutBF16, 16>(cc, mx, mb, p, info, dev, st)
+                    : dispatch_fused<kOutBF16, 128>(cc, mx, mb, p, info, dev, st);
+  };
+  fp8s_status r = run(ch);
+  if (r == FP8S_ERR_SHAPE && ch.splits > 1 && !g_force_bn) {
+    ch.splits = 1;   // the device holds fewer clusters than the estimate assumed: no split
+    r = run(ch);
+  }
+  return r;
+}
+
 fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode_in, int sms, int* bn, int* splits,
                            int* pair) {
-  if (mode_in != FP8S_SCALE_PER_TENSOR && mode_in != FP8S_SCALE_BLOCK && mode_in != FP8S_SCALE_PER_CHANNEL)
+  if (mode_in != FP8S_SCALE_PER_TENSOR && mode_in != FP8S_SCALE_BLOCK && mode_in != FP8S_SCALE_PER_CHANNEL &&
+      mode_in != FP8S_SCALE_BLOCK_UE8M0)
     return FP8S_ERR_DTYPE;
   const fp8s_scale_mode mode = mode_in == FP8S_SCALE_PER_CHANNEL ? FP8S_SCALE_PER_TENSOR : mode_in;
   if (!bn || !splits || !pair) return FP8S_ERR_NULL;
   if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || sms < 1) return FP8S_ERR_SHAPE;
-  if (mode == FP8S_SCALE_BLOCK && K % 128 != 0) return FP8S_ERR_SHAPE;
+  if ((mode == FP8S_SCALE_BLOCK || mode == FP8S_SCALE_BLOCK_UE8M0) && K % 128 != 0) return FP8S_ERR_SHAPE;
   const GemmChoice ch = choose_gemm(M, N, (K + kBK - 1) / kBK, mode, sms);
   *bn = ch.bn;
   *splits = ch.splits;
@@ -813,6 +994,11 @@ fp8s_status fp8s_device_error(fp8s_stream_t stream, int* where) {
   }
   if (where) *where = static_cast<int>(word);
   return word ? FP8S_ERR_DEVICE_TIMEOUT : FP8S_OK;
+}
+
+fp8s_status fp8s_set_exchange_timeout_ns(unsigned long long ns) {
+  g_exchange_timeout_ns.store(ns == 0 ? kWaitTimeoutNs : ns);
+  return FP8S_OK;
 }
 
 int fp8s_version(void) { return kVersion; }

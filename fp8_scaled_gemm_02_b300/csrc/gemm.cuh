@@ -71,8 +71,11 @@ constexpr int kBK = 128;   // K block: 128 E4M3 bytes = one swizzled smem row
 constexpr int kMmaK = 32;  // K of one tcgen05.mma kind::f8f6f4
 
 // Per-channel weights (one sB per output column) run the per-tensor kernel
-// with a per-column epilogue scale.
-enum : int { kModePerTensor = 0, kModeBlock = 1, kModePerChannel = 2 };
+// with a per-column epilogue scale.  kModeUE8 is the block geometry with
+// power-of-two (UE8M0) scales, applied by the tensor core itself
+// (kind::mxf8f6f4.block_scale): the accumulator then spans the whole K range
+// like per-tensor mode, and the epilogue only rounds.
+enum : int { kModePerTensor = 0, kModeBlock = 1, kModePerChannel = 2, kModeUE8 = 3 };
 enum : int { kOutF16 = 0, kOutBF16 = 1 };
 
 struct GemmParams {
@@ -84,16 +87,29 @@ struct GemmParams {
   const float* sb;
   void* c;
   unsigned long long timeout_ns;
+  // fused activation quantization: optional copies of the E4M3 activation
+  // [M][K] and its token-group scales [K/128][M] (written by the CTAs of
+  // tile column 0)
+  uint8_t* qa_out;
+  float* sa_out;
 };
 
-template <int BN, int MODE, bool SPLIT, bool PAIR = false>
+// FR > 0: the fused linear.  A arrives as FP16/BF16 (the output's type) in
+// boxes of FR rows x 128 columns and is quantized per 1x128 token group
+// inside the kernel (block mode only).
+template <int BN, int MODE, bool SPLIT, bool PAIR = false, int FR = 0>
 struct GemmCfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 192 || BN == 256, "BN");
   static_assert(!(SPLIT && PAIR), "a CTA pair does not also split K");
   static_assert(!PAIR || BN >= 64, "a CTA pair holds at least 32 rows of B each");
+  static_assert(!(PAIR && MODE == kModeUE8), "UE8M0 scale factors are staged per CTA");
   // Block mode keeps 64 FP32 accumulators per epilogue thread: BN = 192 and
   // 256 need three and four epilogue warpgroups.
-  static constexpr int kEpiWarps = MODE != kModeBlock ? 8 : BN == 256 ? 16 : BN == 192 ? 12 : 8;
+  // UE8M0 mode with BN = 256 keeps a single TMEM accumulator, which the
+  // epilogue must hand back quickly: four warpgroups of 64 columns load the
+  // whole tile before any store.
+  static constexpr int kEpiWarps = MODE == kModeUE8 ? (BN == 256 ? 16 : 8)
+                                 : MODE != kModeBlock ? 8 : BN == 256 ? 16 : BN == 192 ? 12 : 8;
   static constexpr int kEpiWG = kEpiWarps / 4;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kThreads = 128 + kEpiThreads;
@@ -106,9 +122,15 @@ struct GemmCfg {
   static constexpr int kSeqLoadCols = kLowReg ? 16 : 32;
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;   // output rows per (pair) tile
   static constexpr int kBRows = PAIR ? BN / 2 : BN;     // rows of B this CTA loads
+  static constexpr bool kFused = FR > 0;
+  static_assert(!kFused || (MODE == kModeBlock && !PAIR && BN <= 128 && (FR == 16 || FR == 128)),
+                "fused activation quantization: block mode, single CTAs, 16- or 128-row boxes");
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = kBRows * kBK;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kXBytes = FR * kBK * 2;            // fused: FP16/BF16 activation box
+  static constexpr int kStageBytes = kABytes + kBBytes + kXBytes;
+  static constexpr int kSaSlots = kFused ? 8 : 0;         // fused: ring of per-K-block token scales
+  static constexpr int kSaBytes = kSaSlots * kBM * 4;
   // Split-K partial: 128 rows x BN FP32, rows padded by 4 words so that
   // 16-byte writes of 8 consecutive rows cover all 32 banks.  The outgoing
   // partial aliases the drained operand ring; the incoming slices of up to 7
@@ -117,16 +139,30 @@ struct GemmCfg {
   static constexpr int kStagePitch = BN + 4;
   static constexpr int kStagingBytes = kBM * kStagePitch * 4;
   static constexpr int kRecvBytes = SPLIT ? 112 * kStagePitch * 4 : 0;
-  static constexpr int kStagesRaw = (214 * 1024 - kRecvBytes) / kStageBytes;
+  // UE8M0 scale factors: per group of four K blocks, one 32-bit word (a
+  // byte per K block) per row of A and per row of B.  Warp 3 stages them in
+  // shared memory as tiles of 32 rows x 16 bytes, one per 128 rows of the
+  // operand: row r of a tile holds the words of rows r, 32 + r, 64 + r and
+  // 96 + r of those 128.  The MMA issuer copies each tile into four TMEM
+  // columns (tcgen05.cp ... warpx4).  A ring of kSfSlots groups, each slot
+  // with shared memory and TMEM columns of its own.
+  static constexpr bool kUE8 = MODE == kModeUE8;
+  static constexpr int kSfbTiles = kUE8 ? (BN + 127) / 128 : 0;   // scale tiles of B (one per 128 rows)
+  static constexpr int kSfSlots = kUE8 ? 4 : 0;
+  static constexpr int kSfSlotBytes = 512 * (1 + kSfbTiles);
+  static constexpr int kSfBytes = kSfSlots * kSfSlotBytes;
+  static constexpr int kSfCols = 4 * (1 + kSfbTiles);               // TMEM columns per slot
+  static constexpr int kStagesRaw = (214 * 1024 - kRecvBytes - kSfBytes - kSaBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(!SPLIT || kStages * kStageBytes >= kStagingBytes, "staging fits in the ring");
   // TMEM accumulator buffers: whole tiles (per-tensor) or single K blocks
   // (block mode; narrow tiles get up to 16 so the MMA can run far ahead).
   static constexpr int kNBufMax = MODE == kModeBlock ? 16 : 4;
-  static constexpr int kTmemMax = 512;
+  static constexpr int kTmemMax = 512 - kSfSlots * kSfCols;
   static constexpr int kNBuf = (kTmemMax / BN) > kNBufMax ? kNBufMax : (kTmemMax / BN);
-  static constexpr int kTmemCols = kNBuf * BN;
+  static constexpr int kTmemAccCols = kNBuf * BN;
+  static constexpr int kTmemCols = kTmemAccCols + kSfSlots * kSfCols;
   static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                   : kTmemCols <= 256 ? 256 : 512;  // allocations are powers of two
   static constexpr int kColsPerThread = BN / kEpiWG;
@@ -138,8 +174,9 @@ struct GemmCfg {
   static constexpr int kBatch =
       (MODE == kModeBlock && !kSeqChunks) ? (kBatchRaw > kNBuf / 2 ? kNBuf / 2 : kBatchRaw) : 1;
   static_assert(kBatch >= 1, "batch");
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 1 + 2) + 16;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRecvBytes + kBarBytes;
+  static constexpr int kBarBytes =
+      8 * (2 * kStages + 2 * kNBuf + 1 + 2 + 2 * kSfSlots + (kFused ? kStages + 2 * kSaSlots : 0)) + 16;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRecvBytes + kSfBytes + kSaBytes + kBarBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kTmemCols <= 512, "TMEM columns");
 };
@@ -246,18 +283,25 @@ __device__ __forceinline__ void release_tmem(uint64_t* bar) {
   else ptx::mbar_arrive(bar);
 }
 
-// Sums this CTA's R = 128/S rows over the S partials in rank order (its own
-// in `send`, peer q's in receive slot q < rank ? q : q - 1), rounds and
-// stores them.  S is a template parameter so that the S loads of an output
-// vector are issued together; each thread takes two 4-column vectors per
+// Rows of a split-K tile each rank reduces: the tile's valid rows (all 128
+// unless the tile holds the last rows of M) split evenly over the S ranks;
+// S * R <= 128 always.  A decode batch of a few tokens exchanges a few rows.
+__device__ __forceinline__ int split_rows(const GemmParams& p, int tm, int S) {
+  const int mt = min(kBM, p.M - tm * kBM);
+  return (mt + S - 1) / S;
+}
+
+// Sums this CTA's R rows over the S partials in rank order (its own in
+// `send`, peer q's in receive slot q < rank ? q : q - 1), rounds and stores
+// them.  S is a template parameter so that the S loads of an output vector
+// are issued together; each thread takes two 4-column vectors per
 // iteration.
 template <int BN, int OUT, int S>
 __device__ __forceinline__ void reduce_rows(const float* send, const float* recv, uint32_t rank, int tid, int nthreads,
-                                            int tm, int tn, const GemmParams& p) {
+                                            int tm, int tn, int R, const GemmParams& p) {
   constexpr int kPitch = BN + 4;
   constexpr int kVecPerRow = BN / 4;
-  constexpr int R = kBM / S;
-  constexpr int kTotal = R * kVecPerRow;
+  const int kTotal = R * kVecPerRow;
   uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
   const bool vec_ok = (p.N % 4) == 0;
   const float* src[S];
@@ -322,8 +366,8 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
                                                     const float* recv, uint32_t rank, uint32_t S, int tid,
                                                     int nthreads, int tm, int tn, const GemmParams& p) {
   constexpr int kPitch = BN + 4;
-  const int R = kBM / static_cast<int>(S);
-  const uint32_t slice_bytes = static_cast<uint32_t>(R * kPitch * 4);
+  const int R = split_rows(p, tm, static_cast<int>(S));
+  const uint32_t slice_bytes = static_cast<uint32_t>(R * kPitch * 4);   // a multiple of 16 for every BN
   const int lane = tid & 31;
   ptx::fence_proxy_async_shared();  // this thread's ordinary stores, before the bulk copies read them
   __syncwarp();
@@ -356,9 +400,9 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
     return false;
   }
   switch (S) {
-    case 2: reduce_rows<BN, OUT, 2>(send, recv, rank, tid, nthreads, tm, tn, p); break;
-    case 4: reduce_rows<BN, OUT, 4>(send, recv, rank, tid, nthreads, tm, tn, p); break;
-    default: reduce_rows<BN, OUT, 8>(send, recv, rank, tid, nthreads, tm, tn, p); break;
+    case 2: reduce_rows<BN, OUT, 2>(send, recv, rank, tid, nthreads, tm, tn, R, p); break;
+    case 4: reduce_rows<BN, OUT, 4>(send, recv, rank, tid, nthreads, tm, tn, R, p); break;
+    default: reduce_rows<BN, OUT, 8>(send, recv, rank, tid, nthreads, tm, tn, R, p); break;
   }
   return true;
 }
@@ -368,7 +412,9 @@ __device__ __forceinline__ bool exchange_and_reduce(uint64_t* staged_bar, uint64
 // keeps a ragged tile's loads inside sB; those columns are never stored).
 template <int MODE, int CW>
 __device__ __forceinline__ void scale_chunk(float* v, float pt_scale, float sa, const GemmParams& p, int n0) {
-  if constexpr (MODE == kModePerChannel) {
+  if constexpr (MODE == kModeUE8) {
+    // the tensor core has applied the scales already
+  } else if constexpr (MODE == kModePerChannel) {
 #pragma unroll
     for (int j = 0; j < CW; ++j) v[j] *= sa * __ldg(p.sb + (n0 + j < p.N ? n0 + j : p.N - 1));
   } else {
@@ -377,11 +423,12 @@ __device__ __forceinline__ void scale_chunk(float* v, float pt_scale, float sa, 
   }
 }
 
-template <int BN, int MODE, int OUT, bool SPLIT, bool PAIR>
-__global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
+template <int BN, int MODE, int OUT, bool SPLIT, bool PAIR, int FR = 0>
+__global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmParams p) {
-  using Cfg = GemmCfg<BN, MODE, SPLIT, PAIR>;
+  using Cfg = GemmCfg<BN, MODE, SPLIT, PAIR, FR>;
+  constexpr int DT = OUT;  // fused: the activation has the output's type (kInF16 == kOutF16, kInBF16 == kOutBF16)
   constexpr int TM = Cfg::kTileM;
   constexpr int S_ = Cfg::kStages;
   constexpr int NBUF = Cfg::kNBuf;
@@ -392,16 +439,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + S_ * Cfg::kABytes;
+  uint8_t* smem_x = smem_b + S_ * Cfg::kBBytes;  // fused: FP16/BF16 activation boxes
   float* staging = reinterpret_cast<float*>(smem);  // split-K only: used after the ring has drained
   const float* recv = reinterpret_cast<const float*>(smem + S_ * Cfg::kStageBytes);  // split-K incoming slices
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + S_ * Cfg::kBBytes + Cfg::kRecvBytes);
+  uint8_t* sf_smem = smem + S_ * Cfg::kStageBytes + Cfg::kRecvBytes;  // UE8M0: scale-factor tiles
+  float* sa_ring = reinterpret_cast<float*>(sf_smem + Cfg::kSfBytes);   // fused: [kSaSlots][128] token scales
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sa_ring) + Cfg::kSaBytes);
   uint64_t* empty_bar = full_bar + S_;
   uint64_t* tfull_bar = empty_bar + S_;
   uint64_t* tempty_bar = tfull_bar + NBUF;
   uint64_t* mma_done_bar = tempty_bar + NBUF;
   uint64_t* staged_bar = mma_done_bar + 1;  // split-K: every epilogue warp of this CTA staged its part
   uint64_t* recv_bar = staged_bar + 1;      // split-K: all S-1 incoming slices have landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
+  uint64_t* sf_full_bar = recv_bar + 1;     // UE8M0: a scale-factor slot has been staged
+  uint64_t* sf_empty_bar = sf_full_bar + Cfg::kSfSlots;  // UE8M0: its MMAs are done with it
+  uint64_t* a8_ready_bar = sf_empty_bar + Cfg::kSfSlots;  // fused: stage's E4M3 activation written
+  uint64_t* sa_full_bar = a8_ready_bar + (Cfg::kFused ? S_ : 0);  // fused: a scale slot written
+  uint64_t* sa_free_bar = sa_full_bar + Cfg::kSaSlots;            // fused: a scale slot read by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sa_free_bar + Cfg::kSaSlots);
   volatile uint32_t* pair_bad = tmem_slot + 1;  // CTA pair: the two TMEM allocations disagree
 
   const int warp = threadIdx.x >> 5;
@@ -443,6 +498,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
     ptx::mbar_init(mma_done_bar, 1);
     ptx::mbar_init(staged_bar, Cfg::kEpiWarps);
     ptx::mbar_init(recv_bar, 1);
+    for (int j = 0; j < Cfg::kSfSlots; ++j) {
+      ptx::mbar_init(&sf_full_bar[j], 1);
+      ptx::mbar_init(&sf_empty_bar[j], 1);
+    }
+    if constexpr (Cfg::kFused) {
+      for (int j = 0; j < S_; ++j) ptx::mbar_init(&a8_ready_bar[j], 2);   // the two quantizer warps
+      for (int j = 0; j < Cfg::kSaSlots; ++j) {
+        ptx::mbar_init(&sa_full_bar[j], 2);
+        ptx::mbar_init(&sa_free_bar[j], Cfg::kEpiWarps);
+      }
+    }
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
@@ -453,6 +519,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
       ptx::tmem_alloc<Cfg::kTmemAlloc>(tmem_slot);
       ptx::tmem_relinquish();
     }
+  }
+  if constexpr (Cfg::kFused) {
+    // Rows of the E4M3 activation stages that the quantizer never writes
+    // (past M, or past the FR-row box) stay zero, and the scales of rows past
+    // M stay 1, so the MMA and the promotion see plain zeros there.
+    for (int i = threadIdx.x; i < S_ * Cfg::kABytes / 16; i += Cfg::kThreads)
+      ptx::sts128(ptx::smem_u32(smem_a) + 16u * static_cast<uint32_t>(i), 0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < Cfg::kSaSlots * kBM; i += Cfg::kThreads) sa_ring[i] = 1.0f;
+    ptx::fence_proxy_async_shared();  // the zeros, before the tensor core reads the stages
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -505,6 +580,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
             const uint32_t fb = full0 + 8u * static_cast<uint32_t>(s);
             ptx::tma_load_2d_pair(smem_a + s * Cfg::kABytes, &tmap_a, fb, kb * kBK, tm * TM + prank * kBM);
             ptx::tma_load_2d_pair(smem_b + s * Cfg::kBBytes, &tmap_b, fb, kb * kBK, tn * BN + prank * (BN / 2));
+          } else if constexpr (Cfg::kFused) {
+            // the activation in FP16/BF16 (FR rows, 128 columns = 256 bytes a row)
+            ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kXBytes + Cfg::kBBytes);
+            ptx::tma_load_2d(smem_x + s * Cfg::kXBytes, &tmap_a, &full_bar[s], kb * kBK, tm * kBM);
+            ptx::tma_load_2d(smem_b + s * Cfg::kBBytes, &tmap_b, &full_bar[s], kb * kBK, tn * BN);
           } else {
             ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kStageBytes);
             ptx::tma_load_2d(smem_a + s * Cfg::kABytes, &tmap_a, &full_bar[s], kb * kBK, tm * kBM);
@@ -526,10 +606,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = ptx::idesc_e4m3_f32(TM, BN);
+      constexpr uint32_t idesc = Cfg::kUE8 ? ptx::idesc_mxf8_e4m3_ue8m0(TM, BN) : ptx::idesc_e4m3_f32(TM, BN);
       const uint32_t a0 = ptx::smem_u32(smem_a);
       const uint32_t b0 = ptx::smem_u32(smem_b);
       uint32_t consumed = 0, unit = 0;
+      uint32_t sfg = 0, sf_tmem = 0;  // UE8M0: scale-factor groups consumed; TMEM columns of the current one
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
         for (int i = 0; i < nkb && ok; ++i) {  // i counts K blocks of the tile in issue order
@@ -545,8 +626,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
             }
             ptx::tc_fence_after();
           }
+          if constexpr (Cfg::kUE8) {
+            if ((i & 3) == 0) {
+              // the scale factors of this group of four K blocks: shared memory -> TMEM
+              const uint32_t slot = sfg % Cfg::kSfSlots;
+              if (!ptx::mbar_wait_bounded(&sf_full_bar[slot], (sfg / Cfg::kSfSlots) & 1, p.timeout_ns)) {
+                record_error(kErrMma);
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              const uint32_t src = ptx::smem_u32(sf_smem + slot * Cfg::kSfSlotBytes);
+              sf_tmem = tmem_base + Cfg::kTmemAccCols + slot * Cfg::kSfCols;
+#pragma unroll
+              for (int j = 0; j <= Cfg::kSfbTiles; ++j)
+                ptx::tmem_cp_32x128b_warpx4(sf_tmem + 4 * j, ptx::smem_desc_rows16(src + 512 * j));
+            }
+          }
           const int s = consumed % S_;
-          if (!ptx::mbar_wait_bounded(&full_bar[s], (consumed / S_) & 1, p.timeout_ns)) {
+          if (!ptx::mbar_wait_bounded(&full_bar[s], (consumed / S_) & 1, p.timeout_ns) ||
+              (Cfg::kFused && !ptx::mbar_wait_bounded(&a8_ready_bar[s], (consumed / S_) & 1, p.timeout_ns))) {
             record_error(kErrMma);
             ok = false;
             break;
@@ -560,10 +659,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
             // advance 32 bytes (2 x 16-byte units) along K inside the swizzled row
             const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (i > 0 || k > 0);
             if constexpr (PAIR) ptx::mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
+            else if constexpr (Cfg::kUE8)
+              // byte i % 4 of every scale word belongs to this K block (A's
+              // words in the slot's first four columns, B's after them)
+              ptx::mma_mxf8f6f4_bs(d, adesc + 2 * k, bdesc + 2 * k, ptx::idesc_sf_id(idesc, i & 3), sf_tmem,
+                                   sf_tmem + 4, acc);
             else ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
           }
           if constexpr (PAIR) ptx::mma_commit_pair_mc(&empty_bar[s], 0x3);
           else ptx::mma_commit(&empty_bar[s]);
+          if constexpr (Cfg::kUE8) {
+            if ((i & 3) == 3 || i == nkb - 1) {  // the group's last MMA: its scale slot frees when they complete
+              ptx::mma_commit(&sf_empty_bar[sfg % Cfg::kSfSlots]);
+              ++sfg;
+            }
+          }
           ++consumed;
           const bool unit_done = (MODE == kModeBlock) || i == nkb - 1;
           if (unit_done) {
@@ -577,6 +687,148 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
       if constexpr (PAIR) ptx::mma_commit_pair_mc(mma_done_bar, 0x1);
       else ptx::mma_commit(mma_done_bar);
       if (!ptx::mbar_wait_bounded(mma_done_bar, 0, p.timeout_ns)) record_error(kErrMma);
+    }
+  } else if (Cfg::kFused && (warp == 2 || warp == 3)) {
+    // ------------------------------------ fused activation quantizer
+    // Per stage: the FR-row FP16/BF16 box of A has landed (full barrier).
+    // Each row of the box is one 1x128 token group ([P5] groups, [P2] s3
+    // steps 2-4): a half-warp reads its 256 bytes (8 elements a lane), takes
+    // the amax with four shuffles, s = fl32(amax / 448), and writes the
+    // E4M3 bytes into the stage's A tile in the MMA's 128-byte swizzled
+    // layout (16-byte unit u of row r at unit u ^ (r % 8)), and s into the
+    // slot of the scale ring that the epilogue reads for this K block.
+    // Warp 2 takes rows 0, 1, 4, 5, ..., warp 3 rows 2, 3, 6, 7, ...; rows
+    // past M are skipped (their bytes stay zero, their scales 1).
+    if constexpr (Cfg::kFused) {
+      const int qwarp = warp - 2, half = lane >> 4, hl = lane & 15;
+      uint32_t it = 0, u = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        const int rot = kb_rotation(tm, tn, nkb);
+        const bool copy_out = p.qa_out != nullptr && tn == 0;
+        for (int i = 0; i < nkb; ++i, ++it, ++u) {
+          const int kb = kb_begin + (i + rot < nkb ? i + rot : i + rot - nkb);
+          const int s = it % S_;
+          const uint32_t slot = u % Cfg::kSaSlots;
+          bool got = true;
+          if (lane == 0)
+            got = ptx::mbar_wait_bounded(&full_bar[s], (it / S_) & 1, p.timeout_ns) &&
+                  ptx::mbar_wait_bounded(&sa_free_bar[slot], ((u / Cfg::kSaSlots) & 1) ^ 1, p.timeout_ns);
+          if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
+            if (lane == 0) record_error(kErrProducer);
+            ok = false;
+            break;
+          }
+          const uint32_t xs = ptx::smem_u32(smem_x + s * Cfg::kXBytes);
+          const uint32_t as = ptx::smem_u32(smem_a + s * Cfg::kABytes);
+          float* sa_slot = sa_ring + slot * kBM;
+          for (int r0 = 2 * qwarp; r0 < FR; r0 += 4) {
+            if (tm * kBM + r0 >= p.M) break;  // warp-uniform: later rows are past M too
+            const int r = r0 + half;
+            const int m = tm * kBM + r;
+            const uint4 v = lds128(xs + static_cast<uint32_t>(r * 256 + hl * 16));
+            uint32_t a = amax_bits8(v);
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            const UnitScale us(mag_to_float<DT>(a));
+            const uint2 q8 = quant8<DT>(v, us);
+            if (m < p.M) {
+              const uint32_t unit = static_cast<uint32_t>(hl >> 1) ^ static_cast<uint32_t>(r & 7);
+              const uint32_t dst = as + static_cast<uint32_t>(r * 128) + (unit << 4) + static_cast<uint32_t>((hl & 1) * 8);
+              asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(q8.x), "r"(q8.y) : "memory");
+              if (hl == 0) sa_slot[r] = us.s;
+              if (copy_out) {
+                reinterpret_cast<uint2*>(p.qa_out + static_cast<int64_t>(m) * p.K + kb * kBK)[hl] = q8;
+                if (hl == 0) p.sa_out[static_cast<int64_t>(kb) * p.M + m] = us.s;
+              }
+            }
+          }
+          ptx::fence_proxy_async_shared();  // the E4M3 bytes, before the MMA reads them
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(&a8_ready_bar[s]);
+            ptx::mbar_arrive(&sa_full_bar[slot]);
+          }
+        }
+      }
+    }
+  } else if (warp == 3) {
+    // ----------------------------------------- UE8M0 scale-factor stager
+    // Per tile and group of four K blocks (in the tile's issue order): lane
+    // l builds the scale words of rows l, 32 + l, 64 + l, 96 + l of A's 128
+    // rows and of every 128 rows of B's BN (byte i = the code of the group's
+    // i-th K block; rows past M or N and K blocks past the tile's range get
+    // 127, i.e. 2^0), writes them as 16-byte rows of the slot's tiles and
+    // hands the slot to the MMA issuer.
+    if constexpr (Cfg::kUE8) {
+      const uint8_t* sa8 = reinterpret_cast<const uint8_t*>(p.sa);
+      const uint8_t* sb8 = reinterpret_cast<const uint8_t*>(p.sb);
+      uint32_t sfg = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        const int rot = kb_rotation(tm, tn, nkb);
+        for (int g0 = 0; g0 < nkb; g0 += 4) {
+          const uint32_t slot = sfg % Cfg::kSfSlots;
+          bool free_ok = true;
+          if (lane == 0) free_ok = ptx::mbar_wait_bounded(&sf_empty_bar[slot], ((sfg / Cfg::kSfSlots) & 1) ^ 1,
+                                                          p.timeout_ns);
+          if (!__shfl_sync(0xFFFFFFFFu, free_ok ? 1 : 0, 0)) {
+            if (lane == 0) record_error(kErrMma);
+            ok = false;
+            break;
+          }
+          int kbs[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = g0 + i;
+            kbs[i] = idx < nkb ? kb_begin + (idx + rot < nkb ? idx + rot : idx + rot - nkb) : -1;
+          }
+          const uint32_t dst = ptx::smem_u32(sf_smem + slot * Cfg::kSfSlotBytes) + static_cast<uint32_t>(lane * 16);
+          {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int m = tm * kBM + j * 32 + lane;
+              uint32_t word = 0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t c = (kbs[i] >= 0 && m < p.M) ? __ldg(sa8 + static_cast<int64_t>(kbs[i]) * p.M + m) : 127u;
+                word |= c << (8 * i);
+              }
+              w[j] = word;
+            }
+            ptx::sts128(dst, w[0], w[1], w[2], w[3]);
+          }
+#pragma unroll
+          for (int h = 0; h < Cfg::kSfbTiles; ++h) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int n = tn * BN + h * 128 + j * 32 + lane;
+              const int64_t nb = n / 128;
+              uint32_t word = 0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t c = (kbs[i] >= 0 && n < p.N && n < tn * BN + BN) ? __ldg(sb8 + nb * p.num_kb + kbs[i])
+                                                                                  : 127u;
+                word |= c << (8 * i);
+              }
+              w[j] = word;
+            }
+            ptx::sts128(dst + 512 * (h + 1), w[0], w[1], w[2], w[3]);
+          }
+          ptx::fence_proxy_async_shared();  // these stores, before tcgen05.cp reads them
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sf_full_bar[slot]);
+          ++sfg;
+        }
+      }
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------------- epilogue
@@ -593,7 +845,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
     bool ok = true;
 
     float pt_scale = 0.0f, pt_sa = 0.0f;
-    if constexpr (MODE != kModeBlock) {
+    if constexpr (MODE == kModePerTensor || MODE == kModePerChannel) {
       pt_sa = __ldg(p.sa);
       pt_scale = pt_sa * __ldg(p.sb);
     }
@@ -614,12 +866,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
         }
         ptx::tc_fence_after();
         if constexpr (SPLIT) {
+          const bool staged_row = row_local < split_rows(p, tm, static_cast<int>(S)) * static_cast<int>(S);
 #pragma unroll
           for (int c = 0; c < CPT / CW; ++c) {
             float v[CW];
             tmem_load_chunk<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, v);
             scale_chunk<MODE, CW>(v, pt_scale, pt_sa, p, n_base + c * CW);
-            stage_row<CW>(srow + c * CW, v);
+            if (staged_row) stage_row<CW>(srow + c * CW, v);
           }
           if (!cluster_waited) {  // peers' barriers are initialised from here on
             ptx::cluster_wait();
@@ -628,6 +881,28 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
           if (!exchange_and_reduce<BN, OUT>(staged_bar, recv_bar, staging, recv, rank, S, epi_tid, Cfg::kEpiThreads,
                                             tm, tn, p))
             ok = false;
+        } else if constexpr (Cfg::kUE8) {
+          // The whole row slice is loaded before the buffer is handed back
+          // (with one accumulator buffer, the next tile's MMAs wait for it),
+          // then rounded and stored.
+          uint32_t r[CPT];
+#pragma unroll
+          for (int c = 0; c < CPT / CW; ++c) tmem_load_nowait<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, &r[c * CW]);
+          ptx::tmem_ld_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) release_tmem<PAIR>(&tempty_bar[buf]);
+          if (row < p.M) {
+#pragma unroll
+            for (int c = 0; c < CPT / CW; ++c) {
+              float v[CW];
+#pragma unroll
+              for (int j = 0; j < CW; ++j) v[j] = __uint_as_float(r[c * CW + j]);
+              store_row<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, v);
+            }
+          }
+          ++unit;
+          continue;
         } else {
 #pragma unroll
           for (int c = 0; c < CPT / CW; ++c) {
@@ -702,7 +977,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
         float sa_n[KBT], sb_n[KBT];
 #pragma unroll
         for (int j = 0; j < KBT; ++j) {
-          sa_n[j] = j < nkb ? __ldg(sa_col + static_cast<int64_t>(kb_at(j)) * p.M) : 0.0f;
+          if constexpr (!Cfg::kFused) sa_n[j] = j < nkb ? __ldg(sa_col + static_cast<int64_t>(kb_at(j)) * p.M) : 0.0f;
           sb_n[j] = j < nkb ? __ldg(sb_row + kb_at(j)) : 0.0f;
         }
         for (int kb0 = 0; kb0 < nkb; kb0 += KBT) {
@@ -710,9 +985,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
           float sc[KBT];
 #pragma unroll
           for (int j = 0; j < KBT; ++j) {
-            sc[j] = sa_n[j] * sb_n[j];
+            if constexpr (Cfg::kFused) sc[j] = sb_n[j];   // times the token scale, read below
+            else sc[j] = sa_n[j] * sb_n[j];
             const int kn = kb0 + KBT + j;  // prefetch the next batch's scales
-            sa_n[j] = kn < nkb ? __ldg(sa_col + static_cast<int64_t>(kb_at(kn)) * p.M) : 0.0f;
+            if constexpr (!Cfg::kFused) sa_n[j] = kn < nkb ? __ldg(sa_col + static_cast<int64_t>(kb_at(kn)) * p.M) : 0.0f;
             sb_n[j] = kn < nkb ? __ldg(sb_row + kb_at(kn)) : 0.0f;
           }
           for (int j = 0; j < nbat && ok; ++j) {
@@ -720,6 +996,28 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
             if (!ptx::mbar_wait_bounded(&tfull_bar[u % NBUF], (u / NBUF) & 1, p.timeout_ns)) {
               record_error(kErrEpilogue);
               ok = false;
+            }
+          }
+          if constexpr (Cfg::kFused) {
+            // the token scales of these K blocks, from the quantizer's ring
+            bool got = true;
+            if (lane == 0)
+              for (int j = 0; j < nbat && got && ok; ++j) {
+                const uint32_t u = unit + j;
+                got = ptx::mbar_wait_bounded(&sa_full_bar[u % Cfg::kSaSlots], (u / Cfg::kSaSlots) & 1, p.timeout_ns);
+              }
+            if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
+              if (lane == 0) record_error(kErrEpilogue);
+              ok = false;
+            }
+            if (ok) {
+              __syncwarp();  // lane 0's acquire orders the other lanes' reads too
+#pragma unroll
+              for (int j = 0; j < KBT; ++j)
+                if (j < nbat) sc[j] *= sa_ring[((unit + j) % Cfg::kSaSlots) * kBM + row_local];
+              __syncwarp();
+              if (lane == 0)
+                for (int j = 0; j < nbat; ++j) ptx::mbar_arrive(&sa_free_bar[(unit + j) % Cfg::kSaSlots]);
             }
           }
           if (!ok) break;
@@ -752,7 +1050,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR>::kThreads, 1)
         }
         if (!ok) break;
         if constexpr (SPLIT) {
-          stage_row<CPT>(srow, acc);
+          if (row_local < split_rows(p, tm, static_cast<int>(S)) * static_cast<int>(S)) stage_row<CPT>(srow, acc);
           if (!cluster_waited) {  // peers' barriers are initialised from here on
             ptx::cluster_wait();
             cluster_waited = true;

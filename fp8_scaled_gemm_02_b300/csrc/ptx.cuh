@@ -390,6 +390,63 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// ------------------------------------------- block-scaled MMA (UE8M0)
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T, E4M3 x E4M3 -> F32, with one
+// UE8M0 scale factor per row of A and per row of B for the MMA's 32-wide K
+// slice (scale_vec::1X), read from TMEM at `sfa_tmem` / `sfb_tmem`.
+__device__ __forceinline__ void mma_mxf8f6f4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies 32 rows x 16 bytes of shared memory (described by `src_desc`) into
+// TMEM columns taddr .. taddr+3 of lanes 0-31, and the same data into lanes
+// 32-63, 64-95 and 96-127 (row r -> lane r of every 32-lane quarter, its
+// four 32-bit words -> the four columns).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
+// Shared-memory descriptor of a plain (unswizzled) 32-row x 16-byte tile:
+// rows 16 bytes apart, so the 8-row core matrices are 128 bytes apart
+// (stride byte offset); one core matrix along the 16-byte row (the leading
+// byte offset is unused).  Bits 46-48 hold the fixed value 0b001.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor for kind::mxf8f6f4 block-scaled MMAs: A and B
+// E4M3 (format 0), both K-major, D F32 (implied), UE8M0 scale factors (bit
+// 23), shape M x N (x K=32).  The byte of each 32-bit scale-factor word the
+// MMA uses is chosen per instruction with idesc_sf_id.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3_ue8m0(int M, int N) {
+  return (0u << 7)                                  // A format: E4M3
+         | (0u << 10)                               // B format: E4M3
+         | (0u << 15) | (0u << 16)                  // A, B K-major
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (1u << 23)                               // scale factors: UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+// Scale-factor byte `id` (0-3) of A's (bits 29-30) and B's (bits 4-5) words.
+__host__ __device__ constexpr uint32_t idesc_sf_id(uint32_t idesc, uint32_t id) {
+  return idesc | (id << 4) | (id << 29);
+}
+
+// 16-byte store to this CTA's shared memory.
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // ------------------------------------------------------ conversions
 // Two FP32 values -> two E4M3 bytes (round to nearest even, saturate to
 // +-448); `hi` lands in the upper byte.

@@ -132,6 +132,29 @@ struct UnitPair {
       : yy(ptx::f2_pack(us.y, us.y)), ll(ptx::f2_pack(us.ylo, us.ylo)) {}
 };
 
+// Power-of-two (UE8M0) scales (the "UE8M0 scale format" section of the
+// transformers "Fine-grained FP8" guide: such checkpoints store each scale
+// as an 8-bit biased exponent).  The unit's FP32 scale fl32(amax / 448) (1
+// when amax == 0) is rounded up to the nearest power of two 2^k (the smallest
+// with 2^k >= it; k >= -127, the smallest UE8M0 value), stored as the byte
+// k + 127.  Then 1/s = 2^-k is exact, so x * 2^-k is the correctly rounded
+// quotient fl32(x / s) itself, and the double-word reciprocal's low word is
+// zero: the same element path computes RN(x * 2^-k).
+__device__ __forceinline__ UnitScale ue8m0_unit(float amax, uint32_t* code) {
+  const float s32 = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+  const uint32_t b = __float_as_uint(s32);
+  const int e = static_cast<int>(b >> 23);
+  const uint32_t m = b & 0x7FFFFFu;
+  // a subnormal s32 lies in (0, 2^-126): 2^-126 covers it if it exceeds
+  // 2^-127 (mantissa above 2^22), else the clamp at 2^-127 applies
+  const int k = e == 0 ? (m > (1u << 22) ? -126 : -127) : e - 127 + (m != 0u ? 1 : 0);
+  *code = static_cast<uint32_t>(k + 127);
+  // 2^k (k = -127 is the subnormal 2^-127) and 2^-k (k <= 120: s32 < 2^121)
+  const float s = k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23) : __uint_as_float(1u << 22);
+  const float y = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+  return UnitScale(s, y, false);   // ylo = RN((1 - s*y) * y) = 0
+}
+
 // Two packed 16-bit inputs -> two E4M3 bytes (low input in the low byte),
 // without the sign of a -0 input (see quant4).
 template <int DT>
@@ -249,9 +272,9 @@ constexpr int kTgStages = 3;
 // (programmatic dependent launch can then start them early).
 constexpr int tg_smem_bytes(int gpw) { return 1024 + kTgStages * 8 * gpw * 256 + 64; }
 
-template <int DT, int GPW>
+template <int DT, int GPW, bool UE8 = false>
 __global__ void __launch_bounds__(288, 2)
-    quant_token_group_kernel(const uint8_t* __restrict__ x, uint2* __restrict__ q, float* __restrict__ sa,
+    quant_token_group_kernel(const uint8_t* __restrict__ x, uint2* __restrict__ q, void* __restrict__ sa_out,
                              uint32_t M, uint32_t G, uint32_t num_groups, unsigned long long timeout_ns) {
   static_assert(GPW == 2 || GPW == 4 || GPW == 8 || GPW == 16, "groups per warp");
   constexpr int kTgChunkGroups = 8 * GPW;
@@ -322,11 +345,14 @@ __global__ void __launch_bounds__(288, 2)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);
 
-      UnitScale own(mag_to_float<DT>(mine));
+      uint32_t code = 0;
+      const UnitScale own = UE8 ? ue8m0_unit(mag_to_float<DT>(mine), &code) : UnitScale(mag_to_float<DT>(mine));
       const uint32_t my_group = gw + hl;
       if (lane < GPW && my_group < num_groups) {
         const uint32_t m = my_group / G;
-        sa[static_cast<uint64_t>(my_group - m * G) * M + m] = own.s;
+        const uint64_t at = static_cast<uint64_t>(my_group - m * G) * M + m;
+        if constexpr (UE8) static_cast<uint8_t*>(sa_out)[at] = static_cast<uint8_t>(code);
+        else static_cast<float*>(sa_out)[at] = own.s;
       }
       // Warp-uniform choices, made once per chunk: every group present, and
       // no group needing the IEEE divide (then no per-group branches).
@@ -378,10 +404,10 @@ constexpr int kWbThreads = 32 * (8 * kWbGroups + 1);
 constexpr int kWbBlockBytes = 128 * 128 * 2;
 constexpr int kWbSmemBytes = 1024 + kWbStages * kWbBlockBytes + 256;
 
-template <int DT>
+template <int DT, bool UE8 = false>
 __global__ void __launch_bounds__(kWbThreads, 1)
     quant_weight_block_tma_kernel(const __grid_constant__ CUtensorMap tmap_w, uint2* __restrict__ q,
-                                  float* __restrict__ sb, int N, int KB, int num_blocks,
+                                  void* __restrict__ sb_out, int N, int KB, int num_blocks,
                                   unsigned long long timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -456,7 +482,8 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       a = gmax[(k & 1) * 8];
 #pragma unroll
       for (int i = 1; i < 8; ++i) a = max(a, gmax[(k & 1) * 8 + i]);
-      const UnitScale us(mag_to_float<DT>(a));
+      uint32_t code = 0;
+      const UnitScale us = UE8 ? ue8m0_unit(mag_to_float<DT>(a), &code) : UnitScale(mag_to_float<DT>(a));
       const UnitPair k(us);
       const int r0 = bi * 128 + (t >> 4);
       uint2* qrow = q + static_cast<int64_t>(r0) * row_vec + bj * 16 + (t & 15);
@@ -473,7 +500,11 @@ __global__ void __launch_bounds__(kWbThreads, 1)
         for (int i = 0; i < 8; ++i)
           if (r0 + 16 * i < N) qrow[i * step] = quant8_impl<DT, true>(v[i], us, k);
       }
-      if (t == 0) sb[static_cast<int64_t>(bi) * KB + bj] = us.s;
+      if (t == 0) {
+        const int64_t at = static_cast<int64_t>(bi) * KB + bj;
+        if constexpr (UE8) static_cast<uint8_t*>(sb_out)[at] = static_cast<uint8_t>(code);
+        else static_cast<float*>(sb_out)[at] = us.s;
+      }
     }
   }
   __syncthreads();

@@ -72,7 +72,8 @@ typedef enum { FP8S_F16 = 0, FP8S_BF16 = 1 } fp8s_dtype;
 typedef enum {
   FP8S_SCALE_PER_TENSOR = 0, /* sa, sb each point to one float */
   FP8S_SCALE_BLOCK = 1,      /* sa: [K/128][M] token-group scales, sb: [ceil(N/128)][K/128] block scales */
-  FP8S_SCALE_PER_CHANNEL = 2 /* sa: one float (per-tensor activation), sb: [N] one scale per output channel */
+  FP8S_SCALE_PER_CHANNEL = 2, /* sa: one float (per-tensor activation), sb: [N] one scale per output channel */
+  FP8S_SCALE_BLOCK_UE8M0 = 3  /* as FP8S_SCALE_BLOCK with UE8M0 codes (one byte each): sa [K/128][M], sb [ceil(N/128)][K/128] */
 } fp8s_scale_mode;
 
 /*
@@ -193,11 +194,88 @@ FP8S_API fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int
  *        one float, sb [N] (from fp8_quantize_per_channel);
  *        C[m][n] = RN(acc[m][n] * (sa * sb[n])).       K % 16 == 0.
  *        The same kernels and tiles as per-tensor mode.
+ *   mode FP8S_SCALE_BLOCK_UE8M0 ([P5] block geometry, "UE8M0 scale format"):
+ *        sa [K/128][M] and sb [ceil(N/128)][K/128] UE8M0 codes (bytes, value
+ *        2^(code-127); from the *_ue8m0 quantizers).  The tensor core applies
+ *        them itself (tcgen05.mma kind::mxf8f6f4.block_scale, one scale per
+ *        row per 32-wide K slice, each code repeated over its 128-wide K
+ *        block): C[m][n] = RN(sum_k dec(qa)*2^(ca-127) * dec(qb)*2^(cb-127))
+ *        accumulated in FP32.  K % 128 == 0.  Codes of 255 (NaN) are not
+ *        accepted.
  *   M, N >= 1, K >= 16.  N need not be a multiple of anything.
  */
 FP8S_API fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                             void* c, fp8s_dtype ct, int64_t M, int64_t N, int64_t K,
                             fp8s_scale_mode mode, fp8s_stream_t stream);
+
+/*
+ * fp8_quantize_token_group_ue8m0 / fp8_quantize_weight_block_ue8m0 -- the
+ * two block quantizers with power-of-two scales stored as UE8M0 codes
+ * ([P5] "UE8M0 scale format": checkpoints that keep each scale as an 8-bit
+ * biased exponent, float8_e8m0fnu; the format Blackwell's block-scaled
+ * tensor-core MMA takes).  Units as in fp8_quantize_token_group (1x128
+ * activation groups) and fp8_quantize_weight_block (128x128 weight blocks).
+ * Per unit: s32 = fl32(amax / 448) (1 when amax == 0), rounded UP to the
+ * nearest power of two 2^k (k >= -127); code = k + 127 (value 2^(code-127));
+ * q = E4M3_rne_satfinite(x / 2^k) (the division is exact), so |x / 2^k| <=
+ * 448 still holds and the amax element may land below 448.
+ *   token group:  x [M][K] -> q [M][K], sa_code [K/128][M] bytes (layout of
+ *                 the FP32 sa).  M >= 1, K >= 128, K % 128 == 0.
+ *   weight block: w [N][K] -> q [N][K], sb_code [ceil(N/128)][K/128] bytes.
+ * All pointers device, 16-byte aligned.  One kernel launch each (the same
+ * kernels as the FP32-scale quantizers, with the scale rounded up).
+ */
+FP8S_API fp8s_status fp8_quantize_token_group_ue8m0(const void* x, fp8s_dtype xt, int64_t M, int64_t K,
+                                                    uint8_t* q, uint8_t* sa_code, fp8s_stream_t stream);
+FP8S_API fp8s_status fp8_quantize_weight_block_ue8m0(const void* w, fp8s_dtype wt, int64_t N, int64_t K,
+                                                     uint8_t* q, uint8_t* sb_code, fp8s_stream_t stream);
+
+/*
+ * fp8_e5m2_encode / fp8_e5m2_decode -- the E5M2 format (5 exponent + 2
+ * mantissa bits: [P2] s2 "FP8 formats", [P3] s2), the FP8 variant with the
+ * wider range and coarser steps that the pages name beside E4M3.  Reading
+ * taken where the pages give only the bit split: bias 15, S.11111.00 =
+ * +-infinity, S.11111.xx (xx != 0) = NaN, largest finite value 57344.
+ *   encode: x [numel] FP16/BF16 (xt), device -> q [numel] E5M2 bytes, device:
+ *           round to nearest even; finite values beyond 57344 and
+ *           +-infinity saturate to +-57344; a NaN gives S.11111.11 with the
+ *           input's sign; the sign of zero is kept.  No scaling.
+ *   decode: q [numel] E5M2 bytes, device -> y [numel] FP16/BF16 (yt), device:
+ *           exact (every E5M2 value is an FP16 and a BF16 value); the
+ *           infinity codes give infinities, the NaN codes NaNs.
+ * numel >= 1; all pointers 16-byte aligned.  One kernel launch each (an
+ * HBM-bound stream, 3 bytes of traffic per element).
+ */
+FP8S_API fp8s_status fp8_e5m2_encode(const void* x, fp8s_dtype xt, int64_t numel, uint8_t* q,
+                                     fp8s_stream_t stream);
+FP8S_API fp8s_status fp8_e5m2_decode(const uint8_t* q, int64_t numel, void* y, fp8s_dtype yt,
+                                     fp8s_stream_t stream);
+
+/*
+ * fp8_linear_token_group -- the fused FP8 linear layer: [P2] s3 steps 2-6
+ * with [P5]'s 1x128 token groups on the activation, in ONE kernel.  The
+ * activation arrives unquantized; each CTA of the block-scaled GEMM loads
+ * its FP16/BF16 tiles of x, quantizes every 1x128 group in shared memory
+ * (amax, s = fl32(amax / 448), E4M3(fl32(x / s)), exactly as
+ * fp8_quantize_token_group) and feeds the E4M3 tile to the tensor core,
+ * so the quantized activation never makes a round trip through HBM and the
+ * quantize launch disappears.  The weight is pre-quantized per 128x128 block
+ * (fp8_quantize_weight_block).
+ *   x   [M][K] FP16/BF16 (xt), device.          K >= 128, K % 128 == 0, M, N >= 1.
+ *   qw  [N][K] E4M3, sw [ceil(N/128)][K/128] FP32: the block-quantized weight.
+ *   c   [M][N] output in the activation's type xt, device:
+ *       C = the FP8S_SCALE_BLOCK GEMM of (token-group quantized x, qw, sw).
+ *   qa, sa  both NULL, or qa [M][K] E4M3 and sa [K/128][M] FP32 outputs that
+ *       receive the quantized activation and its scales (byte- and
+ *       bit-identical to fp8_quantize_token_group's).
+ * Designed for decode batches (M <= 128; M <= 16 uses a 16-row activation
+ * box), where the weight stream dominates; any M is correct.  Tile
+ * overrides (fp8s_gemm_override) apply with bn 64 or 128 and no pair.
+ * All pointers 16-byte aligned.  One kernel launch.
+ */
+FP8S_API fp8s_status fp8_linear_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K, const uint8_t* qw,
+                                            const float* sw, int64_t N, void* c, uint8_t* qa, float* sa,
+                                            fp8s_stream_t stream);
 
 /*
  * fp8s_gemm_override -- tuning aid: makes every later fp8_gemm_scaled call on
@@ -248,6 +326,19 @@ FP8S_API const char* fp8s_last_cuda_error(void);
  * FP8S_ERR_DEVICE_TIMEOUT or FP8S_ERR_CUDA.
  */
 FP8S_API fp8s_status fp8s_device_error(fp8s_stream_t stream, int* where);
+
+/*
+ * fp8s_set_exchange_timeout_ns -- test aid for the failure path of the
+ * bounded waits: sets the wall-time limit (ns) of the grid-wide exchange
+ * spin of fp8_quantize_per_tensor for inputs above ~29 MB (whose CTAs stream
+ * their slices, so no asynchronous copy is in flight while they wait);
+ * 0 restores the default of 2 s.  A spin that runs out records 4 in the
+ * device error word (fp8s_device_error) and its CTA carries on, so the call
+ * ends with unspecified output bytes and no hang.  Every other wait keeps
+ * its 2 s limit.  Process-wide; not for production use.  Diagnostic only:
+ * no method step stands behind it.
+ */
+FP8S_API fp8s_status fp8s_set_exchange_timeout_ns(unsigned long long ns);
 
 /* Library version, major*10000 + minor*100 + patch. */
 FP8S_API int fp8s_version(void);

@@ -95,7 +95,7 @@ def test_per_channel_argument_checks(lib):
     g = lib.fp8_gemm_scaled
     assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 8, 8, 24, 2, None) == 2
     assert g(GOOD, GOOD, GOOD, BAD_ALIGN, GOOD, 0, 8, 8, 32, 2, None) == 3
-    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 8, 8, 32, 3, None) == 4
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 8, 8, 32, 4, None) == 4          # no mode 4
 
 
 def test_per_channel_plan_is_the_per_tensor_plan(lib):
@@ -194,3 +194,43 @@ def test_gemm_plan_argument_checks(lib):
     assert lib.fp8s_gemm_plan(128, 128, 128, 5, 148, *args) == 4
     assert lib.fp8s_gemm_plan(128, 128, 128, 1, 0, *args) == 2
     assert lib.fp8s_gemm_plan(128, 128, 128, 1, 148, None, *args[1:]) == 1
+
+
+def test_e5m2_argument_checks(lib):
+    enc, dec = lib.fp8_e5m2_encode, lib.fp8_e5m2_decode
+    assert enc(GOOD, 2, 64, GOOD, None) == 4
+    assert enc(None, 0, 64, GOOD, None) == 1
+    assert enc(GOOD, 0, 0, GOOD, None) == 2
+    assert enc(GOOD, 1, 64, BAD_ALIGN, None) == 3
+    assert dec(GOOD, 64, GOOD, 5, None) == 4
+    assert dec(GOOD, 64, None, 0, None) == 1
+    assert dec(GOOD, -1, GOOD, 0, None) == 2
+    assert dec(BAD_ALIGN, 64, GOOD, 1, None) == 3
+
+
+def test_ue8m0_argument_checks(lib):
+    tg, wb = lib.fp8_quantize_token_group_ue8m0, lib.fp8_quantize_weight_block_ue8m0
+    assert tg(GOOD, 2, 4, 128, GOOD, GOOD, None) == 4
+    assert tg(GOOD, 0, 4, 128, GOOD, None, None) == 1
+    assert tg(GOOD, 0, 4, 200, GOOD, GOOD, None) == 2
+    assert tg(GOOD, 0, 4, 128, GOOD, BAD_ALIGN, None) == 3
+    assert wb(GOOD, 1, 0, 128, GOOD, GOOD, None) == 2
+    assert wb(GOOD, 1, 5, 128, None, GOOD, None) == 1
+    assert wb(GOOD, 1, 5, 256, GOOD, BAD_ALIGN, None) == 3
+    g = lib.fp8_gemm_scaled
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 8, 8, 144, 3, None) == 2      # UE8M0 block mode: K % 128
+    assert g(GOOD, GOOD, GOOD, GOOD, BAD_ALIGN, 1, 8, 8, 128, 3, None) == 3
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 8, 8, 128, 4, None) == 4
+
+
+def test_ue8m0_plan_has_no_cta_pairs(lib):
+    """The UE8M0 mode stages its scale factors per CTA: never a CTA pair,
+    and split-K only up to 192-wide tiles."""
+    for M, N, K in [(16384, 8192, 8192), (4096, 22016, 4096), (128, 4096, 4096), (1, 4096, 11008)]:
+        bn, sp, pr = plan(lib, M, N, K, 3)
+        assert pr == 0 and (sp == 1 or bn <= 192)
+
+
+def test_exchange_timeout_setter(lib):
+    assert lib.fp8s_set_exchange_timeout_ns(5) == 0
+    assert lib.fp8s_set_exchange_timeout_ns(0) == 0

@@ -164,3 +164,36 @@ def test_oracle_sample_is_fixed():
     assert bench.oracle_sample_rows(wl) == bench.oracle_sample_rows(wl) == [149]
     wl = synth.WORKLOADS["llama2_7b_m1"]
     assert bench.oracle_sample_rows(wl) == [1, 1, 1, 1]
+
+
+def test_default_lines_end_with_the_headline():
+    """A plain run prints the decode (unfused vs fused) and UE8M0 lines first
+    and the largest block-scaled workload last."""
+    import bench
+
+    class Args:
+        workload = None
+        modes = ""
+        gpus = 1
+
+    lines = bench.lines_of(Args())
+    assert [(a.workload, a.modes) for a in lines][-1] == ("outlier_16384x8192x8192", "")
+    assert ("llama2_7b_m1", "block,fused") in [(a.workload, a.modes) for a in lines]
+    Args.workload = "llama2_7b_m8"
+    assert [(a.workload, a.modes) for a in bench.lines_of(Args())] == [("llama2_7b_m8", "")]
+
+
+def test_fused_and_ue8m0_plans():
+    import bench
+
+    class Args:
+        workload = "llama2_7b_m1"
+        modes = "block,fused,block_ue8m0"
+
+    plan = bench.kernel_plan(bench.workload_of(Args()))
+    names = {mode: [k[0] for k in ks] for lin, mode, ks in plan if lin.name == "o"}
+    assert names["fused"] == ["quant_weight_block", "linear_fused"]
+    assert names["block_ue8m0"] == ["quant_token_group_ue8m0", "quant_weight_block_ue8m0", "gemm_block_ue8m0"]
+    fused = [ks for lin, mode, ks in plan if lin.name == "o" and mode == "fused"][0]
+    M, N, K = 1, 4096, 4096
+    assert fused[1][2] == M * K * 2 + N * K + 4 * 32 * 32 + 2 * M * N and fused[1][3] == 2 * M * N * K

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import TD, host, no_device_error, out_bits_to_f64, to_dev  # noqa: F401
+from gpu_util import TD, Guarded, host, no_device_error, out_bits_to_f64, to_dev  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -23,20 +23,29 @@ F = pytest.importorskip("fp8_scaled_gemm_02_b300")
 
 def run_linear(a_bits, w_bits, in_dt, out_dt, mode, rows=None):
     """Quantize A and W on the GPU, run the GEMM; check bytes/scales against
-    the oracle, then the output against the oracle GEMM on `rows`."""
+    the oracle, then the output against the oracle GEMM on `rows`.  Every
+    output sits inside canary bands and starts as poison (0xFF bytes), so a
+    store past a ragged tile's edge or an element left unwritten fails."""
     a, w = to_dev(a_bits, in_dt), to_dev(w_bits, in_dt)
+    (M, K), N = a_bits.shape, w_bits.shape[0]
+    gqa, gqw = Guarded((M, K), torch.uint8), Guarded((N, K), torch.uint8)
     if mode == "block":
-        qa, sa = F.fp8_quantize_token_group(a)
-        qw, sw = F.fp8_quantize_weight_block(w)
+        gsa, gsw = Guarded((K // 128, M), torch.float32), Guarded(((N + 127) // 128, K // 128), torch.float32)
+        qa, sa = F.fp8_quantize_token_group(a, q=gqa.t, sa=gsa.t)
+        qw, sw = F.fp8_quantize_weight_block(w, q=gqw.t, sb=gsw.t)
         oqa, osa = oracle.quantize_token_group(a_bits, in_dt)
         oqw, osw = oracle.quantize_weight_block(w_bits, in_dt)
     else:
-        qa, sa = F.fp8_quantize_per_tensor(a)
-        qw, sw = F.fp8_quantize_per_tensor(w)
+        gsa, gsw = Guarded((1,), torch.float32), Guarded((1,), torch.float32)
+        qa, sa = F.fp8_quantize_per_tensor(a, q=gqa.t, scale=gsa.t)
+        qw, sw = F.fp8_quantize_per_tensor(w, q=gqw.t, scale=gsw.t)
         oqa, osa = oracle.quantize_per_tensor(a_bits, in_dt)
         oqw, osw = oracle.quantize_per_tensor(w_bits, in_dt)
-    c = F.fp8_gemm_scaled(qa, sa, qw, sw, out_dtype=TD[out_dt], mode=mode)
+    gc = Guarded((M, N), TD[out_dt])
+    c = F.fp8_gemm_scaled(qa, sa, qw, sw, out_dtype=TD[out_dt], mode=mode, c=gc.t)
     torch.cuda.synchronize()
+    for g in (gqa, gqw, gsa, gsw, gc):
+        g.check()
     assert np.array_equal(host(qa), oqa) and np.array_equal(host(qw), oqw), "operand bytes differ"
     if mode == "block":
         assert np.array_equal(host(sa), osa) and np.array_equal(host(sw), osw), "scales differ"
@@ -125,3 +134,13 @@ def test_workload_outlier_full_size():
     lin = wl.linears[0]
     run_linear(synth.activation(wl, lin), synth.weight(wl, lin), "f16", "f16", "block",
                rows=_sample_rows(lin.M, n=24))
+
+
+def test_workload_outlier_per_tensor_full_size():
+    """The full-size outlier shape with per-tensor scaling: the automatically
+    chosen CTA-pair (cta_group::2) tiles, on sampled output rows."""
+    wl = synth.WORKLOADS["outlier_16384x8192x8192"]
+    lin = wl.linears[0]
+    assert F.fp8s_gemm_plan(lin.M, lin.N, lin.K, "per_tensor")[2], "expected the CTA-pair configuration"
+    run_linear(synth.activation(wl, lin), synth.weight(wl, lin), "f16", "f16", "per_tensor",
+               rows=_sample_rows(lin.M, n=24, seed=1))

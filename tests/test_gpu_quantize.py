@@ -4,14 +4,17 @@ FP32 scales must be bit-exact.
 Cases: several tiles with ragged edges, single-row / single-group minima,
 all-zero and negative-zero units, exhaustive coverage of every FP16 and BF16
 amax pattern, every FP16/BF16 input pattern at a set of scales, and the
-full-size activation and weight tensors of the workloads."""
+full-size activation and weight tensors of the workloads.  Every output
+sits inside canary bands and starts as poison (0xFF bytes, never a code or
+scale a finite input produces): a store outside an output or an element
+left unwritten fails the test."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from gpu_util import host, no_device_error, to_dev  # noqa: F401
+from gpu_util import Guarded, host, no_device_error, to_dev  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -19,7 +22,12 @@ F = pytest.importorskip("fp8_scaled_gemm_02_b300")
 
 
 def check_token_group(bits, dtype):
-    qa, sa = F.fp8_quantize_token_group(to_dev(bits, dtype))
+    M, K = bits.shape
+    gq, gs = Guarded((M, K), torch.uint8), Guarded((K // 128, M), torch.float32)
+    qa, sa = F.fp8_quantize_token_group(to_dev(bits, dtype), q=gq.t, sa=gs.t)
+    torch.cuda.synchronize()
+    gq.check()
+    gs.check()
     oq, os_ = oracle.quantize_token_group(bits, dtype)
     q, s = host(qa), host(sa)
     assert np.array_equal(s.view(np.uint32), os_.view(np.uint32)), f"scales differ at {np.argwhere(s != os_)[:5]}"
@@ -28,7 +36,12 @@ def check_token_group(bits, dtype):
 
 
 def check_weight_block(bits, dtype):
-    qw, sw = F.fp8_quantize_weight_block(to_dev(bits, dtype))
+    N, K = bits.shape
+    gq, gs = Guarded((N, K), torch.uint8), Guarded(((N + 127) // 128, K // 128), torch.float32)
+    qw, sw = F.fp8_quantize_weight_block(to_dev(bits, dtype), q=gq.t, sb=gs.t)
+    torch.cuda.synchronize()
+    gq.check()
+    gs.check()
     oq, os_ = oracle.quantize_weight_block(bits, dtype)
     assert np.array_equal(host(sw).view(np.uint32), os_.view(np.uint32))
     bad = np.argwhere(host(qw) != oq)
@@ -36,7 +49,11 @@ def check_weight_block(bits, dtype):
 
 
 def check_per_tensor(bits, dtype):
-    q, s = F.fp8_quantize_per_tensor(to_dev(bits, dtype))
+    gq, gs = Guarded(bits.shape, torch.uint8), Guarded((1,), torch.float32)
+    q, s = F.fp8_quantize_per_tensor(to_dev(bits, dtype), q=gq.t, scale=gs.t)
+    torch.cuda.synchronize()
+    gq.check()
+    gs.check()
     oq, os_ = oracle.quantize_per_tensor(bits, dtype)
     assert host(s)[0].view(np.uint32) == np.float32(os_).view(np.uint32)
     assert np.array_equal(host(q), oq)
