@@ -7,6 +7,10 @@ every linear of the workload and every scaling mode it uses:
   per-tensor mode: per-tensor quantize of A and of W, GEMM
   per_channel (opt-in with --modes): per-tensor quantize of A, per-channel
                    (one scale per output row) quantize of W, GEMM
+  block_fp8w / fused_fp8w (weights held in FP8, quantized once before any
+                   timing, as a model's weights are at load time): per
+                   linear the token-group quantize of A and the GEMM, or
+                   the fused linear alone
   per_tensor_static (delayed scaling, opt-in with --modes): A quantized with
                    the scale held from earlier steps while its amax goes
                    into a ring of HIST_LEN slots, per-tensor quantize of W,
@@ -63,12 +67,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 HIST_LEN = 16        # amax-history ring of the delayed-scaling mode
 HIST_MARGIN = 0      # the recipe's margin (DelayedScaling(margin=0, interval=4))
-MODES = ("block", "per_tensor", "per_tensor_static", "per_channel", "block_ue8m0", "fused")
+MODES = ("block", "per_tensor", "per_tensor_static", "per_channel", "block_ue8m0", "fused", "block_fp8w", "fused_fp8w")
+# Modes whose weights are held in FP8: quantized once when the buffers are
+# set up (a model's weights are quantized at load time and stored in FP8),
+# so a step is the per-token work only: the activation's token-group
+# quantization and the GEMM, or the fused linear alone.
+FP8W_MODES = ("block_fp8w", "fused_fp8w")
 # A plain run prints one line per entry, the headline (the largest workload,
 # block-scaled with FP32 scales) last: a decode batch of one token through
-# the unfused and the fused linear, and the headline shape with power-of-two
-# (UE8M0) scales on the tensor core's block-scaled MMA.
-DEFAULT_LINES = (("llama2_7b_m1", "block,fused"), (DEFAULT_WORKLOAD, "block_ue8m0"), (DEFAULT_WORKLOAD, ""))
+# the unfused and the fused linear (weights held in FP8), and the headline
+# shape with power-of-two (UE8M0) scales on the tensor core's block-scaled
+# MMA.
+DEFAULT_LINES = (("llama2_7b_m1", "block_fp8w,fused_fp8w"), (DEFAULT_WORKLOAD, "block_ue8m0"), (DEFAULT_WORKLOAD, ""))
 
 
 def parse_args():
@@ -156,6 +166,11 @@ def kernel_plan(wl):
                 # the activation is read once in 16 bits and quantized inside the GEMM
                 ks = [("quant_weight_block", "hbm", N * K * 3 + 4 * nb * kbn, 0),
                       ("linear_fused", None, M * K * 2 + N * K + 4 * nb * kbn + 2 * M * N, 2 * M * N * K)]
+            elif mode == "block_fp8w":
+                ks = [("quant_token_group", "hbm", M * K * 3 + 4 * M * kbn, 0),
+                      ("gemm_block", None, M * K + N * K + 4 * M * kbn + 4 * nb * kbn + 2 * M * N, 2 * M * N * K)]
+            elif mode == "fused_fp8w":
+                ks = [("linear_fused", None, M * K * 2 + N * K + 4 * nb * kbn + 2 * M * N, 2 * M * N * K)]
             elif mode == "block":
                 ks = [("quant_token_group", "hbm", M * K * 3 + 4 * M * (K // 128), 0),
                       ("quant_weight_block", "hbm", N * K * 3 + 4 * ((N + 127) // 128) * (K // 128), 0),
@@ -367,7 +382,7 @@ def run_ours(args):
             b = {"qa": torch.empty((M, K), dtype=torch.uint8, device=dev),
                  "qw": torch.empty((N, K), dtype=torch.uint8, device=dev),
                  "c": torch.empty((M, N), dtype=out_t, device=dev)}
-            if mode in ("block", "fused"):
+            if mode in ("block", "fused", "block_fp8w", "fused_fp8w"):
                 b["sa"] = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
                 b["sw"] = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
             elif mode == "block_ue8m0":
@@ -378,6 +393,9 @@ def run_ours(args):
                 b["sw"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
             if mode == "per_channel":
                 b["sw"] = torch.empty(N, dtype=torch.float32, device=dev)
+            if mode in FP8W_MODES:
+                # the weight, quantized once (load time), outside every timed region
+                F.fp8_quantize_weight_block(bufs["w"][lin.name], q=b["qw"], sb=b["sw"])
             if mode == "per_tensor_static":
                 # the held scale starts at the activation's own (calibrated) scale
                 F.fp8_quantize_per_tensor(bufs["a"][lin.K], q=b["qa"], scale=b["sa"])
@@ -399,6 +417,14 @@ def run_ours(args):
                 ca = None
                 cw = lambda w=w, b=b: F.fp8_quantize_weight_block(w, q=b["qw"], sb=b["sw"])
                 cg = lambda a=a, b=b: F.fp8_linear_token_group(a, b["qw"], b["sw"], c=b["c"])
+            elif mode == "fused_fp8w":
+                ca, cw = None, None
+                cg = lambda a=a, b=b: F.fp8_linear_token_group(a, b["qw"], b["sw"], c=b["c"])
+            elif mode == "block_fp8w":
+                ca = lambda a=a, b=b: F.fp8_quantize_token_group(a, q=b["qa"], sa=b["sa"])
+                cw = None
+                cg = lambda b=b: F.fp8_gemm_scaled(b["qa"], b["sa"], b["qw"], b["sw"], out_dtype=out_t,
+                                                   mode="block", c=b["c"])
             elif mode == "block_ue8m0":
                 ca = lambda a=a, b=b: F.fp8_quantize_token_group_ue8m0(a, q=b["qa"], sa=b["sa"])
                 cw = lambda w=w, b=b: F.fp8_quantize_weight_block_ue8m0(w, q=b["qw"], sb=b["sw"])
@@ -441,11 +467,10 @@ def run_ours(args):
         are independent), then the GEMM runs on `main` after both, followed
         by the linear's post-GEMM calls (the delayed-scaling update)."""
         for ca, cw, cg, post in linear_calls(r):
-            if ca is None:   # fused: the GEMM quantizes the activation itself
-                cw()
-                cg()
-                for c in post:
-                    c()
+            if ca is None or cw is None:   # fused, or weights held in FP8: one chain on `main`
+                for c in (ca, cw, cg, *post):
+                    if c is not None:
+                        c()
                 continue
             ev_fork = torch.cuda.Event()
             ev_fork.record(main)
@@ -571,6 +596,8 @@ def run_ours(args):
         # one pinned output buffer per linear and input set, so that the
         # read-back of step i never shares host memory with that of step i+1
         pin_c = [[torch.empty((lin.M, lin.N), dtype=out_t).pin_memory() for lin, _, _ in plan] for _ in range(R)]
+        if all(m in FP8W_MODES for m in wl.modes):
+            pin_w = {}   # weights held in FP8 on the device: a step uploads activations only
         h2d = sum(t.numel() * 2 for t in pin_a.values()) + sum(t.numel() * 2 for t in pin_w.values())
         d2h = sum(t.numel() * 2 for t in pin_c[0])
         up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -751,8 +778,12 @@ def oracle_step_sample(wl):
             if mode == "per_tensor_static":
                 s_held = oracle.scale_from_history(np.float32([oracle.amax(a, wl.in_dtype)]), 0)
                 hist = np.zeros(HIST_LEN, np.float32)
+            if mode in FP8W_MODES:   # the weight is quantized once, outside the timed step
+                qw, sw = oracle.quantize_weight_block(w, wl.in_dtype)
             t = time.perf_counter()
-            if mode in ("block", "fused"):
+            if mode in FP8W_MODES:
+                qa, sa = oracle.quantize_token_group(a, wl.in_dtype)
+            elif mode in ("block", "fused"):
                 qa, sa = oracle.quantize_token_group(a, wl.in_dtype)
                 qw, sw = oracle.quantize_weight_block(w, wl.in_dtype)
             elif mode == "block_ue8m0":
@@ -771,7 +802,7 @@ def oracle_step_sample(wl):
                 qw, sw = oracle.quantize_per_tensor(w, wl.in_dtype)
             tq = time.perf_counter() - t
             t = time.perf_counter()
-            if mode in ("block", "fused", "block_ue8m0"):
+            if mode in ("block", "fused", "block_ue8m0") or mode in FP8W_MODES:
                 oracle.gemm_block(qa, sa, qw, sw, rows=np.arange(rows))
             elif mode == "per_channel":
                 oracle.gemm_per_channel(qa, sa, qw, sw, rows=np.arange(rows))

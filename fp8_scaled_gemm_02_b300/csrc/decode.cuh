@@ -1,0 +1,417 @@
+// decode.cuh -- the block-scaled FP8 GEMM for decode batches (M <= 32 tokens),
+// computed transposed: C^T = W . A^T.
+//
+// Method: the block-scaled linear of the transformers "Fine-grained FP8"
+// guide (1x128 token groups, 128x128 weight blocks) with FP32 promotion per
+// 128-wide K block, as in gemm.cuh; only the operand roles change.  A decode
+// batch has few tokens and a weight of megabytes, so the weight tile is the
+// MMA's 128-row operand (A of tcgen05.mma) and the tokens are its N = MT
+// columns (MT = 16 or 32, rows past M zero).  Per K block a stage holds 16 KB
+// of weight and MT x 128 bytes of activation (instead of 16 + 16 KB with the
+// tokens as rows), the TMEM partial is 128 x MT, and the promotion of a K
+// block is MT columns per thread: the weight stream sets the pace.
+//
+//   warp 0      TMA producer: 128x128-byte weight tiles and MT x 128-byte
+//               E4M3 activation tiles (or, fused, M x 128 FP16/BF16
+//               activation boxes on a barrier of their own, so that their
+//               quantization overlaps the weight tile's flight), 128-byte
+//               swizzle, a STAGES-deep ring.
+//   warp 1      MMA issuer: tcgen05.mma kind::f8f6f4, M = 128, N = MT, four
+//               per K block, a fresh TMEM buffer per K block.
+//   warp 2      TMEM allocation; fused: warps 2 and 3 quantize the activation
+//               (warp 2 the even stages of the ring, warp 3 the odd ones;
+//               each row of the box is a 1x128 token group, quantized into
+//               the stage's swizzled E4M3 tile, its scale into a ring the
+//               epilogue reads).
+//   warps 4-7   epilogue: thread = one weight row n of the tile (its lane
+//               quarter of TMEM), MT token columns; per K block it adds
+//               partial[n][m] * sa[kb][m] * sb[n/128][kb] into FP32 pairs.
+// Split-K: the S CTAs of a cluster share the tile, each a K range; the FP32
+// partials are exchanged through distributed shared memory (rank r owns
+// weight rows [r*128/S, (r+1)*128/S)) and summed in rank order, so results
+// are deterministic; no global scratch memory.  Output C[m][n] is written
+// transposed: for a fixed token the 32 lanes of a warp write 32 consecutive
+// columns.
+//
+// Shared memory stays near 100 KB and TMEM at MT * 8 columns, so two CTAs fit
+// on an SM and a grid of up to two CTAs per SM is resident at once.  Every
+// wait is bounded as in gemm.cuh.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace fp8s {
+
+template <int MT, bool SPLIT, bool FUSED>
+struct DecCfg {
+  static_assert(MT == 16 || MT == 32, "token columns per MMA");
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kThreads = 128 + 32 * kEpiWarps;
+  static constexpr int kWBytes = kBM * kBK;                 // 128 weight rows x one K block
+  static constexpr int kXBytes = MT * kBK;                  // E4M3 activation rows
+  static constexpr int kX16Bytes = FUSED ? MT * kBK * 2 : 0;  // fused: FP16/BF16 activation box (M <= MT rows)
+  static constexpr int kStageBytes = kWBytes + kXBytes + kX16Bytes;
+  static constexpr int kPitch = MT + 4;                     // staging row pitch (floats): 16-byte rows
+  static constexpr int kStagingBytes = kBM * kPitch * 4;
+  static constexpr int kRecvBytes = SPLIT ? 112 * kPitch * 4 : 0;
+  static constexpr int kSaSlots = FUSED ? 8 : 0;            // fused: token scales per K block
+  static constexpr int kSaBytes = kSaSlots * MT * 4;
+  static constexpr int kBudget = 104 * 1024;               // two CTAs per SM
+  static constexpr int kStagesRaw = (kBudget - kRecvBytes - kSaBytes - 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(!SPLIT || kStages * kStageBytes >= kStagingBytes, "staging fits in the ring");
+  static constexpr int kNBuf = 8;
+  static constexpr int kTmemCols = kNBuf * MT;               // 128 or 256: a power of two
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 3 + (FUSED ? 2 * kStages + 2 * kSaSlots : 0)) + 16;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRecvBytes + kSaBytes + kBarBytes;
+  static_assert(kSmemBytes <= 113 * 1024, "shared memory: two CTAs per SM");
+  static constexpr int kCtasPerSm = 2;
+};
+
+// Sums this CTA's R weight rows over the S partials in rank order and stores
+// them transposed, C[m][tn*128 + row] for m < M (consecutive threads take
+// consecutive rows, so each store of a warp covers 32 consecutive columns).
+template <int MT, int OUT, int S>
+__device__ __forceinline__ void dec_reduce(const float* send, const float* recv, uint32_t rank, int tid, int tn,
+                                           const GemmParams& p) {
+  constexpr int kPitch = MT + 4;
+  constexpr int R = kBM / S;
+  uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
+  const float* src[S];
+#pragma unroll
+  for (int q = 0; q < S; ++q)
+    src[q] = q == static_cast<int>(rank) ? send + static_cast<int>(rank) * R * kPitch
+                                         : recv + (q < static_cast<int>(rank) ? q : q - 1) * R * kPitch;
+  const int mmax = p.M < MT ? p.M : MT;
+  for (int idx = tid; idx < R * mmax; idx += 32 * DecCfg<MT, true, false>::kEpiWarps) {
+    const int m = idx / R, rr = idx - (idx / R) * R;
+    float v[S];
+#pragma unroll
+    for (int q = 0; q < S; ++q) v[q] = src[q][rr * kPitch + m];
+    float acc = v[0];
+#pragma unroll
+    for (int q = 1; q < S; ++q) acc += v[q];
+    const int n = tn * kBM + static_cast<int>(rank) * R + rr;
+    if (n < p.N) C[static_cast<int64_t>(m) * p.N + n] = one_out<OUT>(acc);
+  }
+}
+
+template <int MT, int OUT, bool SPLIT, bool FUSED>
+__global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <= 128 registers
+    fp8_decode_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                      const GemmParams p) {
+  using Cfg = DecCfg<MT, SPLIT, FUSED>;
+  constexpr int S_ = Cfg::kStages;
+  constexpr int NBUF = Cfg::kNBuf;
+  constexpr int DT = OUT;  // fused: the activation has the output's type
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* w_ring = smem;
+  uint8_t* x_ring = w_ring + S_ * Cfg::kWBytes;
+  uint8_t* x16_ring = x_ring + S_ * Cfg::kXBytes;
+  float* staging = reinterpret_cast<float*>(smem);  // split-K: after the ring has drained
+  const float* recv = reinterpret_cast<const float*>(smem + S_ * Cfg::kStageBytes);
+  float* sa_ring = reinterpret_cast<float*>(smem + S_ * Cfg::kStageBytes + Cfg::kRecvBytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sa_ring) + Cfg::kSaBytes);
+  uint64_t* empty_bar = full_bar + S_;
+  uint64_t* tfull_bar = empty_bar + S_;
+  uint64_t* tempty_bar = tfull_bar + NBUF;
+  uint64_t* mma_done_bar = tempty_bar + NBUF;
+  uint64_t* staged_bar = mma_done_bar + 1;
+  uint64_t* recv_bar = staged_bar + 1;
+  uint64_t* x8_ready_bar = recv_bar + 1;                          // fused: stage's E4M3 rows written
+  uint64_t* xfull_bar = x8_ready_bar + (FUSED ? S_ : 0);          // fused: stage's activation box landed
+  uint64_t* sa_full_bar = xfull_bar + (FUSED ? S_ : 0);           // fused: a scale slot written
+  uint64_t* sa_free_bar = sa_full_bar + Cfg::kSaSlots;            // fused: a scale slot read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sa_free_bar + Cfg::kSaSlots);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t rank = 0, S = 1;
+  if constexpr (SPLIT) {
+    rank = ptx::cluster_ctarank();
+    S = ptx::cluster_nctarank();
+  }
+  const int tn = static_cast<int>(blockIdx.x / S);   // one weight tile per cluster
+  const int kb_begin = static_cast<int>((static_cast<int64_t>(rank) * p.num_kb) / S);
+  const int kb_end = static_cast<int>((static_cast<int64_t>(rank + 1) * p.num_kb) / S);
+  const int nkb = kb_end - kb_begin;  // >= 1: the host keeps S <= num_kb
+  const int rot = tn % nkb;           // spread the shared activation's L2 requests over K blocks
+  auto kb_at = [&](int i) { return kb_begin + (i + rot < nkb ? i + rot : i + rot - nkb); };
+
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmap_w);
+    ptx::tma_prefetch_desc(&tmap_x);
+    for (int s = 0; s < S_; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < NBUF; ++b) {
+      ptx::mbar_init(&tfull_bar[b], 1);
+      ptx::mbar_init(&tempty_bar[b], Cfg::kEpiWarps);
+    }
+    ptx::mbar_init(mma_done_bar, 1);
+    ptx::mbar_init(staged_bar, Cfg::kEpiWarps);
+    ptx::mbar_init(recv_bar, 1);
+    if constexpr (FUSED) {
+      for (int s = 0; s < S_; ++s) {
+        ptx::mbar_init(&x8_ready_bar[s], 1);   // the quantizer warp of that use of the stage
+        ptx::mbar_init(&xfull_bar[s], 1);
+      }
+      for (int j = 0; j < Cfg::kSaSlots; ++j) {
+        ptx::mbar_init(&sa_full_bar[j], 1);
+        ptx::mbar_init(&sa_free_bar[j], Cfg::kEpiWarps);
+      }
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc<Cfg::kTmemCols>(tmem_slot);
+    ptx::tmem_relinquish();
+  }
+  if constexpr (FUSED) {
+    // activation rows past M are never written by the quantizer: they stay
+    // zero, and their token scales 0 (the products they meet are zero)
+    for (int i = threadIdx.x; i < S_ * Cfg::kXBytes / 16; i += Cfg::kThreads)
+      ptx::sts128(ptx::smem_u32(x_ring) + 16u * static_cast<uint32_t>(i), 0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < Cfg::kSaSlots * MT; i += Cfg::kThreads) sa_ring[i] = 0.0f;
+    ptx::fence_proxy_async_shared();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if constexpr (SPLIT) ptx::cluster_arrive_relaxed();  // peers' barriers: waited for before the exchange
+  bool cluster_waited = !SPLIT;
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  ptx::griddep_wait();  // the previous kernel's writes (our operands) are visible from here on
+  ptx::griddep_launch();
+
+  // fused: the box holds the M token rows (M <= MT), 256 bytes each
+  const uint32_t x16_box_bytes = static_cast<uint32_t>(p.M < MT ? p.M : MT) * kBK * 2u;
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int kb = kb_at(i);
+        const int s = i % S_;
+        if (!ptx::mbar_wait_bounded(&empty_bar[s], ((i / S_) & 1) ^ 1, p.timeout_ns)) {
+          record_error(kErrProducer);
+          break;
+        }
+        if constexpr (FUSED) {
+          ptx::mbar_arrive_expect_tx(&xfull_bar[s], x16_box_bytes);
+          ptx::tma_load_2d(x16_ring + s * Cfg::kX16Bytes, &tmap_x, &xfull_bar[s], kb * kBK, 0);
+          ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes);
+        } else {
+          ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes + Cfg::kXBytes);
+          ptx::tma_load_2d(x_ring + s * Cfg::kXBytes, &tmap_x, &full_bar[s], kb * kBK, 0);
+        }
+        ptx::tma_load_2d(w_ring + s * Cfg::kWBytes, &tmap_w, &full_bar[s], kb * kBK, tn * kBM);
+        ++issued;
+      }
+      // every issued load lands before the CTA may exit
+      for (int j = issued > S_ ? issued - S_ : 0; j < issued; ++j) {
+        if (!ptx::mbar_wait_bounded(&full_bar[j % S_], (j / S_) & 1, p.timeout_ns)) record_error(kErrProducer);
+        if (FUSED && !ptx::mbar_wait_bounded(&xfull_bar[j % S_], (j / S_) & 1, p.timeout_ns))
+          record_error(kErrProducer);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBM, MT);
+      const uint32_t w0 = ptx::smem_u32(w_ring), x0 = ptx::smem_u32(x_ring);
+      for (int i = 0; i < nkb; ++i) {
+        const int buf = i % NBUF, s = i % S_;
+        if (!ptx::mbar_wait_bounded(&tempty_bar[buf], ((i / NBUF) & 1) ^ 1, p.timeout_ns) ||
+            !ptx::mbar_wait_bounded(&full_bar[s], (i / S_) & 1, p.timeout_ns) ||
+            (FUSED && !ptx::mbar_wait_bounded(&x8_ready_bar[s], (i / S_) & 1, p.timeout_ns))) {
+          record_error(kErrMma);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint64_t adesc = ptx::smem_desc_sw128_kmajor(w0 + s * Cfg::kWBytes);
+        const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(x0 + s * Cfg::kXBytes);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * MT);
+#pragma unroll
+        for (int k = 0; k < kBK / kMmaK; ++k) ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+        ptx::mma_commit(&empty_bar[s]);
+        ptx::mma_commit(&tfull_bar[buf]);
+      }
+      ptx::mma_commit(mma_done_bar);
+      if (!ptx::mbar_wait_bounded(mma_done_bar, 0, p.timeout_ns)) record_error(kErrMma);
+    }
+  } else if (FUSED && (warp == 2 || warp == 3)) {
+    // --------------------------------------- fused activation quantizer
+    // Per stage: the M-row box of x has landed (the weight tile may still be
+    // in flight).  Each row is one 1x128 token group ([P5] groups, [P2] s3
+    // steps 2-4), quantized by quant_box16_rows sixteen rows at a time into
+    // the stage's swizzled E4M3 tile, its scale into the ring slot of this K
+    // block.  Each stage of the ring belongs to one warp (warp 2 the even
+    // stages, warp 3 the odd ones), so every barrier of a stage sees its
+    // phases waited for and arrived on in order by one warp.
+    if constexpr (FUSED) {
+      const int qwarp = warp - 2;
+      const bool copy_out = p.qa_out != nullptr && tn == 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S_;
+        if ((s & 1) != qwarp) continue;
+        const int kb = kb_at(i);
+        const int slot = i % Cfg::kSaSlots;
+        bool got = true;
+        if (lane == 0)
+          got = ptx::mbar_wait_bounded(&xfull_bar[s], (i / S_) & 1, p.timeout_ns) &&
+                ptx::mbar_wait_bounded(&sa_free_bar[slot], ((i / Cfg::kSaSlots) & 1) ^ 1, p.timeout_ns);
+        if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
+          if (lane == 0) record_error(kErrProducer);
+          break;
+        }
+        const uint32_t xs = ptx::smem_u32(x16_ring + s * Cfg::kX16Bytes);
+        const uint32_t as = ptx::smem_u32(x_ring + s * Cfg::kXBytes);
+        uint8_t* qo = copy_out ? p.qa_out + static_cast<int64_t>(kb) * kBK : nullptr;
+        float* so = copy_out ? p.sa_out + static_cast<int64_t>(kb) * p.M : nullptr;
+        for (int r0 = 0; r0 < MT && r0 < p.M; r0 += 16)
+          quant_box16_rows<DT>(xs, as, r0, p.M, lane, sa_ring + slot * MT, qo, p.K, so);
+        ptx::fence_proxy_async_shared();  // the E4M3 bytes, before the MMA reads them
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&x8_ready_bar[s]);
+          ptx::mbar_arrive(&sa_full_bar[slot]);
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ----------------------------------------------------------- epilogue
+    const int epi_tid = threadIdx.x - 128;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;               // weight row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float* sb_row = p.sb + static_cast<int64_t>(tn) * p.num_kb;   // the tile is one weight block row
+    float2 acc2[MT / 2];
+#pragma unroll
+    for (int j = 0; j < MT / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
+    bool ok = true;
+    // token scales of the next K block (unfused: from global memory, one K
+    // block ahead; the tokens past M get 0)
+    float sa_n[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) sa_n[m] = 0.0f;
+    float sb_n = __ldg(sb_row + kb_at(0));
+    if constexpr (!FUSED) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) sa_n[m] = m < p.M ? __ldg(p.sa + static_cast<int64_t>(kb_at(0)) * p.M + m) : 0.0f;
+    }
+    for (int i = 0; i < nkb && ok; ++i) {
+      float sa_c[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) sa_c[m] = sa_n[m];
+      const float sb_c = sb_n;
+      if (i + 1 < nkb) {
+        const int kn = kb_at(i + 1);
+        sb_n = __ldg(sb_row + kn);
+        if constexpr (!FUSED) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m) sa_n[m] = m < p.M ? __ldg(p.sa + static_cast<int64_t>(kn) * p.M + m) : 0.0f;
+        }
+      }
+      const int buf = i % NBUF;
+      if (!ptx::mbar_wait_bounded(&tfull_bar[buf], (i / NBUF) & 1, p.timeout_ns)) {
+        record_error(kErrEpilogue);
+        ok = false;
+        break;
+      }
+      if constexpr (FUSED) {
+        const int slot = i % Cfg::kSaSlots;
+        bool got = true;
+        if (lane == 0) got = ptx::mbar_wait_bounded(&sa_full_bar[slot], (i / Cfg::kSaSlots) & 1, p.timeout_ns);
+        if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
+          if (lane == 0) record_error(kErrEpilogue);
+          ok = false;
+          break;
+        }
+        __syncwarp();  // lane 0's acquire orders the other lanes' reads too
+#pragma unroll
+        for (int m = 0; m < MT; ++m) sa_c[m] = sa_ring[slot * MT + m];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sa_free_bar[slot]);
+      }
+      ptx::tc_fence_after();
+      uint32_t part[MT];
+#pragma unroll
+      for (int c = 0; c < MT; c += 16) tmem_load_nowait<16>(tmem_base + lane_off + static_cast<uint32_t>(buf * MT + c), &part[c]);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty_bar[buf]);
+#pragma unroll
+      for (int m = 0; m < MT; m += 2) promote2(acc2[m / 2], part[m], part[m + 1], make_float2(sa_c[m] * sb_c, sa_c[m + 1] * sb_c));
+    }
+    if (ok) {
+      if constexpr (SPLIT) {
+        float* srow = staging + row * Cfg::kPitch;
+#pragma unroll
+        for (int j = 0; j < MT / 2; j += 2)
+          *reinterpret_cast<float4*>(srow + 2 * j) = make_float4(acc2[j].x, acc2[j].y, acc2[j + 1].x, acc2[j + 1].y);
+        if (!cluster_waited) {
+          ptx::cluster_wait();
+          cluster_waited = true;
+        }
+        // push each peer's rows into its receive buffer (as gemm.cuh's split-K)
+        constexpr int kPitch = Cfg::kPitch;
+        const int R = kBM / static_cast<int>(S);
+        const uint32_t slice_bytes = static_cast<uint32_t>(R * kPitch * 4);
+        ptx::fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(staged_bar);
+        if (epi_tid == 0) {
+          if (!ptx::mbar_wait_bounded(staged_bar, 0, p.timeout_ns)) {
+            record_error(kErrEpilogue);
+            ok = false;
+          } else {
+            ptx::mbar_arrive_expect_tx(recv_bar, (S - 1) * slice_bytes);
+            const uint32_t send0 = ptx::smem_u32(staging), recv0 = ptx::smem_u32(recv), rbar = ptx::smem_u32(recv_bar);
+            for (uint32_t k = 1; k < S; ++k) {
+              const uint32_t q = (rank + k) % S;
+              const uint32_t slot = rank < q ? rank : rank - 1;
+              ptx::bulk_copy_to_peer(ptx::mapa(recv0 + slot * slice_bytes, q), send0 + q * slice_bytes, slice_bytes,
+                                     ptx::mapa(rbar, q));
+            }
+          }
+        }
+        if (ptx::mbar_wait_bounded(recv_bar, 0, p.timeout_ns)) {
+          switch (S) {
+            case 2: dec_reduce<MT, OUT, 2>(staging, recv, rank, epi_tid, tn, p); break;
+            case 4: dec_reduce<MT, OUT, 4>(staging, recv, rank, epi_tid, tn, p); break;
+            default: dec_reduce<MT, OUT, 8>(staging, recv, rank, epi_tid, tn, p); break;
+          }
+        } else {
+          record_error(kErrEpilogue);
+        }
+      } else {
+        const int n = tn * kBM + row;
+        if (n < p.N) {
+          uint16_t* C = reinterpret_cast<uint16_t*>(p.c);
+#pragma unroll
+          for (int m = 0; m < MT; m += 2) {
+            if (m < p.M) C[static_cast<int64_t>(m) * p.N + n] = one_out<OUT>(acc2[m / 2].x);
+            if (m + 1 < p.M) C[static_cast<int64_t>(m + 1) * p.N + n] = one_out<OUT>(acc2[m / 2].y);
+          }
+        }
+      }
+    }
+  }
+
+  if (!cluster_waited) ptx::cluster_wait();  // every thread waits out its split-K arrival before the last barrier
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc<Cfg::kTmemCols>(tmem_base);
+  }
+  if constexpr (SPLIT) ptx::cluster_sync_all();  // no CTA leaves while a peer may touch its shared memory
+}
+
+}  // namespace fp8s

@@ -18,6 +18,7 @@
 
 #include "../../include/fp8sgemm.h"
 #include "codec.cuh"
+#include "decode.cuh"
 #include "gemm.cuh"
 #include "quantize.cuh"
 
@@ -487,7 +488,9 @@ int max_active_clusters(KernelT kern, int threads, int smem, int splits, int dev
     if (it != cache.end()) return it->second;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(splits * (sms / splits)), 1, 1);
+  // a grid of one cluster per SM: the count is not capped below what a
+  // kernel with several CTAs per SM can hold
+  cfg.gridDim = dim3(static_cast<unsigned>(splits * sms), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cudaLaunchAttribute attr[1];
@@ -556,6 +559,10 @@ double kb_compute_us(int bn, int mode, bool pair) {
   return bn == 256 ? 0.475 : bn == 192 ? 0.40 : bn == 128 ? 0.343 : 0.33;
 }
 
+// Tensor-core time of one K block of a 128 x bn tile: four MMAs of
+// 128 clocks per 256 columns, never below 64 clocks each (measured), ~1.9 GHz.
+double kb_mma_us(int bn) { return 4.0 * std::max(64.0, 128.0 * bn / 256.0) / 1.9e3; }
+
 double estimate_us(int64_t M, int64_t N, int64_t KB, int mode, int sms, int bn, int s, bool pair) {
   const int64_t tile_m = pair ? 2 * kBM : kBM;
   const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
@@ -564,7 +571,13 @@ double estimate_us(int64_t M, int64_t N, int64_t KB, int mode, int sms, int bn, 
   const int64_t waves = (tiles + clusters - 1) / clusters;
   const int64_t nkb = (KB + s - 1) / s;
   const double kb_bytes = 16384.0 + (pair ? bn * 64.0 : bn * 128.0);  // per CTA per K block
-  const double kb_us = std::max(kb_compute_us(bn, mode, pair), kb_bytes / 85e3);
+  double compute = kb_compute_us(bn, mode, pair);
+  if (mode == FP8S_SCALE_BLOCK && M < kBM) {
+    // the promotion runs only in the warps whose 32 rows hold a row of M
+    const double live = static_cast<double>((M + 31) / 32) / 4.0;
+    compute = std::max(kb_mma_us(bn), compute * live);
+  }
+  const double kb_us = std::max(compute, kb_bytes / 85e3);
   double t = static_cast<double>(waves) * static_cast<double>(nkb) * kb_us;
   const double l2_bytes = static_cast<double>(tiles) * csize * static_cast<double>(nkb) * kb_bytes;
   const double hbm_bytes = static_cast<double>(M) * KB * 128 + static_cast<double>(N) * KB * 128 + 2.0 * M * N;
@@ -572,7 +585,8 @@ double estimate_us(int64_t M, int64_t N, int64_t KB, int mode, int sms, int bn, 
   return t + 2.5 + (s > 1 ? 4.0 : 0.0) + (pair ? 0.7 : 0.0);  // a pair also waits on a cluster barrier to start
 }
 
-GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms, int max_bn = 256, int min_bn = 32) {
+GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms, int max_bn = 256, int min_bn = 32,
+                       int max_split_bn = 192) {
   GemmChoice best;
   double best_t = 1e300;
   const int bns[] = {256, 192, 128, 64, 32};
@@ -580,7 +594,7 @@ GemmChoice choose_gemm(int64_t M, int64_t N, int64_t KB, int mode, int sms, int 
   for (int bn : bns) {
     if (bn > max_bn || bn < min_bn) continue;
     for (int s = 1; s <= 8; s *= 2) {
-      if (s > KB || (s > 1 && bn > 192)) continue;
+      if (s > KB || (s > 1 && bn > max_split_bn)) continue;
       const int64_t tiles = tm * ((N + bn - 1) / bn);
       // split-K needs one tile per cluster (with slack for GPC packing)
       if (s > 1 && tiles > (sms / s) * 7 / 8) continue;
@@ -606,8 +620,10 @@ template <int MODE, int OUT>
 fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                           const DeviceInfo& info, int dev, cudaStream_t st) {
   if (ch.pair) {
-    if constexpr (MODE == kModeUE8) {
-      return FP8S_ERR_SHAPE;  // scale factors are staged per CTA: no CTA pairs
+    if constexpr (MODE == kModeBlock || MODE == kModeUE8) {
+      // the block modes' pairs share B by multicast and keep single-CTA MMAs: 256-wide tiles only
+      if (ch.bn != 256) return FP8S_ERR_SHAPE;
+      return launch_gemm_cfg<256, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
     } else {
       switch (ch.bn) {
         case 64: return launch_gemm_cfg<64, MODE, OUT, false, true>(ma, mb, p, 2, info, dev, st);
@@ -637,8 +653,82 @@ fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUt
   }
 }
 
-// The fused linear: block mode, single-CTA tiles of 64 or 128 columns, with
-// or without split-K; FR-row activation boxes.
+// ---------------------------------------------------------- decode GEMM
+// Block-scaled GEMMs of up to 32 tokens run transposed (decode.cuh): one
+// cluster of S CTAs per 128-row weight tile, S the largest power of two up to
+// 8 that keeps every CTA resident at once (two per SM, one for the fused
+// variant) and at least one K block per CTA.
+constexpr int kDecodeMaxM = 32;
+
+template <int MT, int OUT, bool SPLIT, bool FUSED>
+fp8s_status launch_decode_cfg(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, int splits,
+                              const DeviceInfo& info, int dev, cudaStream_t st) {
+  using Cfg = DecCfg<MT, SPLIT, FUSED>;
+  auto kern = fp8_decode_kernel<MT, OUT, SPLIT, FUSED>;
+  static bool attr_set[kMaxDevices] = {};
+  if (fp8s_status s = ensure_smem_attr(kern, Cfg::kSmemBytes, attr_set)) return s;
+  if constexpr (SPLIT) {
+    const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, splits, dev, info.sms);
+    if (cmax < p.tiles_n) return FP8S_ERR_SHAPE;   // every cluster must be resident (they exchange partials)
+  }
+  return launch_ex(kern, static_cast<unsigned>(p.tiles_n * splits), Cfg::kThreads, Cfg::kSmemBytes, st,
+                   SPLIT ? splits : 1, mw, mx, p);
+}
+
+template <int MT, int OUT, bool FUSED>
+fp8s_status dispatch_decode(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, const DeviceInfo& info,
+                            int dev, cudaStream_t st) {
+  constexpr int kPerSm = DecCfg<MT, true, FUSED>::kCtasPerSm;
+  int s = 8;
+  while (s > 1 && (s > p.num_kb || static_cast<int64_t>(p.tiles_n) * s > kPerSm * static_cast<int64_t>(info.sms))) s /= 2;
+  for (; s > 1; s /= 2) {
+    const fp8s_status r = s == 8   ? launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 8, info, dev, st)
+                          : s == 4 ? launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 4, info, dev, st)
+                                   : launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 2, info, dev, st);
+    if (r != FP8S_ERR_SHAPE) return r;   // else: fewer clusters fit than the count assumed
+  }
+  return launch_decode_cfg<MT, OUT, false, FUSED>(mw, mx, p, 1, info, dev, st);
+}
+
+// qa/x: the E4M3 activation (unfused) or the FP16/BF16 one (fused).
+template <bool FUSED>
+fp8s_status run_decode(const void* act, const uint8_t* qw, const float* sa, const float* sw, void* c, fp8s_dtype ct,
+                       int64_t M, int64_t N, int64_t K, uint8_t* qa_out, float* sa_out, const DeviceInfo& info,
+                       int dev, cudaStream_t st) {
+  const int mt = M <= 16 ? 16 : 32;
+  CUtensorMap mw, mx;
+  if (fp8s_status s = tensor_map_e4m3(qw, N, K, kBM, dev, &mw)) return s;
+  if constexpr (FUSED) {
+    // the box covers the M token rows only (the kernel expects M * 256 bytes)
+    if (fp8s_status s = tensor_map_2d(act, M, K, 2, static_cast<int>(M), kBK, false, dev, &mx)) return s;
+  } else {
+    if (fp8s_status s = tensor_map_e4m3(static_cast<const uint8_t*>(act), M, K, mt, dev, &mx)) return s;
+  }
+  GemmParams p{};
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_kb = static_cast<int>(K / kBK);
+  p.tiles_m = 1;
+  p.tiles_n = static_cast<int>((N + kBM - 1) / kBM);
+  p.num_tiles = p.tiles_n;
+  p.group_m = 1;
+  p.sa = sa;
+  p.sb = sw;
+  p.c = c;
+  p.timeout_ns = kWaitTimeoutNs;
+  p.qa_out = qa_out;
+  p.sa_out = sa_out;
+  if (ct == FP8S_F16)
+    return mt == 16 ? dispatch_decode<16, kOutF16, FUSED>(mw, mx, p, info, dev, st)
+                    : dispatch_decode<32, kOutF16, FUSED>(mw, mx, p, info, dev, st);
+  return mt == 16 ? dispatch_decode<16, kOutBF16, FUSED>(mw, mx, p, info, dev, st)
+                  : dispatch_decode<32, kOutBF16, FUSED>(mw, mx, p, info, dev, st);
+}
+
+// The fused linear: block mode, single-CTA tiles of 64 or 128 columns (with
+// or without split-K) or 192 columns (split-K only with 16-row boxes);
+// FR-row activation boxes.
 template <int OUT, int FR>
 fp8s_status dispatch_fused(const GemmChoice& ch, const CUtensorMap& mx, const CUtensorMap& mb, const GemmParams& p,
                            const DeviceInfo& info, int dev, cudaStream_t st) {
@@ -646,12 +736,16 @@ fp8s_status dispatch_fused(const GemmChoice& ch, const CUtensorMap& mx, const CU
     switch (ch.bn) {
       case 64: return launch_gemm_cfg<64, kModeBlock, OUT, true, false, FR>(mx, mb, p, ch.splits, info, dev, st);
       case 128: return launch_gemm_cfg<128, kModeBlock, OUT, true, false, FR>(mx, mb, p, ch.splits, info, dev, st);
+      case 192:
+        if constexpr (FR == 16) return launch_gemm_cfg<192, kModeBlock, OUT, true, false, FR>(mx, mb, p, ch.splits, info, dev, st);
+        return FP8S_ERR_SHAPE;
       default: return FP8S_ERR_SHAPE;
     }
   }
   switch (ch.bn) {
     case 64: return launch_gemm_cfg<64, kModeBlock, OUT, false, false, FR>(mx, mb, p, 1, info, dev, st);
     case 128: return launch_gemm_cfg<128, kModeBlock, OUT, false, false, FR>(mx, mb, p, 1, info, dev, st);
+    case 192: return launch_gemm_cfg<192, kModeBlock, OUT, false, false, FR>(mx, mb, p, 1, info, dev, st);
     default: return FP8S_ERR_SHAPE;
   }
 }
@@ -826,13 +920,15 @@ fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* q
   cudaStream_t st = as_stream(stream);
 
   const int64_t KB = (K + kBK - 1) / kBK;
+  if (mode == FP8S_SCALE_BLOCK && !per_col && M <= kDecodeMaxM && !g_force_bn)
+    return run_decode<false>(qa, qb, sa, sb, c, ct, M, N, K, nullptr, nullptr, info, dev, st);
   GemmChoice ch = choose_gemm(M, N, KB, mode, info.sms);
   if (g_force_bn) {
     ch.bn = g_force_bn;
     ch.splits = g_force_splits > 0 ? g_force_splits : 1;
     ch.pair = g_force_pair != 0;
     if (ch.splits > KB) return FP8S_ERR_SHAPE;
-    if (ch.pair && mode == FP8S_SCALE_BLOCK_UE8M0) return FP8S_ERR_SHAPE;
+
   }
   const int bn = ch.bn;
   const int tile_m = ch.pair ? 2 * kBM : kBM;
@@ -894,13 +990,19 @@ fp8s_status fp8_linear_token_group(const void* x, fp8s_dtype xt, int64_t M, int6
   cudaStream_t st = as_stream(stream);
 
   const int64_t KB = K / kBK;
-  GemmChoice ch = choose_gemm(M, N, KB, FP8S_SCALE_BLOCK, info.sms, 128, 64);  // the fused kernel's tile widths
+  if (M <= kDecodeMaxM && !g_force_bn)
+    return run_decode<true>(x, qw, nullptr, sw, c, xt, M, N, K, qa, sa, info, dev, st);
+  // the fused kernel's tile widths: 64, 128 and 192 (split-K at 192 only with
+  // 16-row activation boxes, M <= 16)
+  const int fr = M <= 16 ? 16 : 128;   // rows of the activation box: M <= 16 needs only 16
+  GemmChoice ch = choose_gemm(M, N, KB, FP8S_SCALE_BLOCK, info.sms, 192, 64, fr == 16 ? 192 : 128);
   if (g_force_bn) {
     ch.bn = g_force_bn;
     ch.splits = g_force_splits > 0 ? g_force_splits : 1;
-    if (g_force_pair || (ch.bn != 64 && ch.bn != 128) || ch.splits > KB) return FP8S_ERR_SHAPE;
+    if (g_force_pair || (ch.bn != 64 && ch.bn != 128 && ch.bn != 192) || (ch.bn == 192 && ch.splits > 1 && fr != 16) ||
+        ch.splits > KB)
+      return FP8S_ERR_SHAPE;
   }
-  const int fr = M <= 16 ? 16 : 128;   // rows of the activation box: M <= 16 needs only 16
   CUtensorMap mx, mb;
   if (fp8s_status s = tensor_map_2d(x, M, K, 2, fr, kBK, false, dev, &mx)) return s;
   if (fp8s_status s = tensor_map_e4m3(qw, N, K, ch.bn, dev, &mb)) return s;

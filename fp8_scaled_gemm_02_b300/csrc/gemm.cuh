@@ -102,7 +102,7 @@ struct GemmCfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 192 || BN == 256, "BN");
   static_assert(!(SPLIT && PAIR), "a CTA pair does not also split K");
   static_assert(!PAIR || BN >= 64, "a CTA pair holds at least 32 rows of B each");
-  static_assert(!(PAIR && MODE == kModeUE8), "UE8M0 scale factors are staged per CTA");
+  // (UE8M0 pairs share B by multicast: the scale factors stay per CTA)
   // Block mode keeps 64 FP32 accumulators per epilogue thread: BN = 192 and
   // 256 need three and four epilogue warpgroups.
   // UE8M0 mode with BN = 256 keeps a single TMEM accumulator, which the
@@ -120,10 +120,20 @@ struct GemmCfg {
   static constexpr bool kSeqChunks = MODE == kModeBlock && kEpiWarps >= 12;
   // Columns of a K block's partial loaded per wait.
   static constexpr int kSeqLoadCols = kLowReg ? 16 : 32;
+  // PAIR: two CTAs of a cluster share a 256-row tile.  Per-tensor modes
+  // issue cta_group::2 MMAs over both CTAs (kPairMma); the two block modes
+  // keep single-CTA MMAs (the FP32 path's per-K-block TMEM hand-off and the
+  // UE8M0 scale factors stay inside one CTA) and share the B tile instead:
+  // each CTA loads half of it with a TMA multicast into both CTAs' shared
+  // memory (kMcB).
+  static constexpr bool kMcB = PAIR && (MODE == kModeBlock || MODE == kModeUE8);
+  static constexpr bool kPairMma = PAIR && !kMcB;
+  static_assert(!kMcB || BN == 256, "B multicast pairs: 256-wide tiles");
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;   // output rows per (pair) tile
-  static constexpr int kBRows = PAIR ? BN / 2 : BN;     // rows of B this CTA loads
+  static constexpr int kBRows = kPairMma ? BN / 2 : BN;  // rows of B this CTA's shared memory holds
   static constexpr bool kFused = FR > 0;
-  static_assert(!kFused || (MODE == kModeBlock && !PAIR && BN <= 128 && (FR == 16 || FR == 128)),
+  static_assert(!kFused || (MODE == kModeBlock && !PAIR && (BN <= 128 || (BN == 192 && (!SPLIT || FR == 16))) &&
+                             (FR == 16 || FR == 128)),
                 "fused activation quantization: block mode, single CTAs, 16- or 128-row boxes");
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = kBRows * kBK;
@@ -136,9 +146,12 @@ struct GemmCfg {
   // partial aliases the drained operand ring; the incoming slices of up to 7
   // peers (at most 112 rows in all) have a buffer of their own.
   static_assert(!SPLIT || BN <= 192, "split-K exchanges a 128 x BN partial in one pass");
+  // A fused kernel with 16-row activation boxes serves M <= 16: its partial
+  // has at most 16 valid rows, which is all it stages and exchanges.
+  static constexpr int kPartRows = (FR > 0 && FR < kBM) ? FR : kBM;
   static constexpr int kStagePitch = BN + 4;
-  static constexpr int kStagingBytes = kBM * kStagePitch * 4;
-  static constexpr int kRecvBytes = SPLIT ? 112 * kStagePitch * 4 : 0;
+  static constexpr int kStagingBytes = kPartRows * kStagePitch * 4;
+  static constexpr int kRecvBytes = SPLIT ? (kPartRows - kPartRows / 8) * kStagePitch * 4 : 0;
   // UE8M0 scale factors: per group of four K blocks, one 32-bit word (a
   // byte per K block) per row of A and per row of B.  Warp 3 stages them in
   // shared memory as tiles of 32 rows x 16 bytes, one per 128 rows of the
@@ -148,7 +161,7 @@ struct GemmCfg {
   // with shared memory and TMEM columns of its own.
   static constexpr bool kUE8 = MODE == kModeUE8;
   static constexpr int kSfbTiles = kUE8 ? (BN + 127) / 128 : 0;   // scale tiles of B (one per 128 rows)
-  static constexpr int kSfSlots = kUE8 ? 4 : 0;
+  static constexpr int kSfSlots = kUE8 ? (SPLIT ? 4 : 8) : 0;   // split-K: the ring also stages the partial
   static constexpr int kSfSlotBytes = 512 * (1 + kSfbTiles);
   static constexpr int kSfBytes = kSfSlots * kSfSlotBytes;
   static constexpr int kSfCols = 4 * (1 + kSfbTiles);               // TMEM columns per slot
@@ -175,7 +188,7 @@ struct GemmCfg {
       (MODE == kModeBlock && !kSeqChunks) ? (kBatchRaw > kNBuf / 2 ? kNBuf / 2 : kBatchRaw) : 1;
   static_assert(kBatch >= 1, "batch");
   static constexpr int kBarBytes =
-      8 * (2 * kStages + 2 * kNBuf + 1 + 2 + 2 * kSfSlots + (kFused ? kStages + 2 * kSaSlots : 0)) + 16;
+      8 * (2 * kStages + 2 * kNBuf + 1 + 2 + 2 * kSfSlots + (kFused ? 2 * kStages + 2 * kSaSlots : 0)) + 16;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRecvBytes + kSfBytes + kSaBytes + kBarBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kTmemCols <= 512, "TMEM columns");
@@ -258,12 +271,41 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* out) {
   for (int j = 0; j < W; ++j) out[j] = __uint_as_float(r[j]);
 }
 
-// acc[0..1] += {p0, p1} * sc: one packed FMA for two accumulators (each half
-// rounds exactly like fmaf).
-__device__ __forceinline__ void promote2(float* acc, uint32_t p0, uint32_t p1, float sc) {
-  const uint64_t r = ptx::f2_fma(ptx::f2_pack(__uint_as_float(p0), __uint_as_float(p1)), ptx::f2_pack(sc, sc),
-                                 ptx::f2_pack(acc[0], acc[1]));
-  ptx::f2_unpack(r, acc[0], acc[1]);
+// acc += {p0, p1} * sc: one packed FMA for two accumulators (each half rounds
+// exactly like fmaf).  The accumulators are kept as FP32 pairs (float2), so
+// the packed FMA needs no moves to form its operands.
+__device__ __forceinline__ void promote2(float2& acc, uint32_t p0, uint32_t p1, float2 sc) {
+  acc = __ffma2_rn(make_float2(__uint_as_float(p0), __uint_as_float(p1)), sc, acc);
+}
+
+// As store_row, for W values held as W/2 FP32 pairs.
+template <int OUT, int W>
+__device__ __forceinline__ void store_row2(uint16_t* __restrict__ crow, int n0, int N, bool vec_ok, const float2* v) {
+  if (vec_ok && n0 + W <= N) {
+#pragma unroll
+    for (int j = 0; j < W / 2; j += 4) {
+      uint4 pk;
+      pk.x = pack_out<OUT>(v[j + 0].x, v[j + 0].y);
+      pk.y = pack_out<OUT>(v[j + 1].x, v[j + 1].y);
+      pk.z = pack_out<OUT>(v[j + 2].x, v[j + 2].y);
+      pk.w = pack_out<OUT>(v[j + 3].x, v[j + 3].y);
+      *reinterpret_cast<uint4*>(crow + n0 + 2 * j) = pk;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < W / 2; ++j) {
+      if (n0 + 2 * j < N) crow[n0 + 2 * j] = one_out<OUT>(v[j].x);
+      if (n0 + 2 * j + 1 < N) crow[n0 + 2 * j + 1] = one_out<OUT>(v[j].y);
+    }
+  }
+}
+
+// Writes W consecutive FP32 values, held as W/2 pairs, of one staging row.
+template <int W>
+__device__ __forceinline__ void stage_row2(float* srow, const float2* v) {
+#pragma unroll
+  for (int j = 0; j < W / 2; j += 2)
+    *reinterpret_cast<float4*>(srow + 2 * j) = make_float4(v[j].x, v[j].y, v[j + 1].x, v[j + 1].y);
 }
 
 // Writes W consecutive FP32 values of one staging row (16-byte stores).
@@ -454,7 +496,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
   uint64_t* sf_full_bar = recv_bar + 1;     // UE8M0: a scale-factor slot has been staged
   uint64_t* sf_empty_bar = sf_full_bar + Cfg::kSfSlots;  // UE8M0: its MMAs are done with it
   uint64_t* a8_ready_bar = sf_empty_bar + Cfg::kSfSlots;  // fused: stage's E4M3 activation written
-  uint64_t* sa_full_bar = a8_ready_bar + (Cfg::kFused ? S_ : 0);  // fused: a scale slot written
+  uint64_t* xfull_bar = a8_ready_bar + (Cfg::kFused ? S_ : 0);    // fused: stage's FP16/BF16 box landed
+  uint64_t* sa_full_bar = xfull_bar + (Cfg::kFused ? S_ : 0);     // fused: a scale slot written
   uint64_t* sa_free_bar = sa_full_bar + Cfg::kSaSlots;            // fused: a scale slot read by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sa_free_bar + Cfg::kSaSlots);
   volatile uint32_t* pair_bad = tmem_slot + 1;  // CTA pair: the two TMEM allocations disagree
@@ -470,7 +513,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
     S = ptx::cluster_nctarank();
   }
   if constexpr (PAIR) prank = ptx::cluster_ctarank();
-  const bool leader = prank == 0;
+  const bool leader = !Cfg::kPairMma || prank == 0;   // issues the MMAs
   const int csize = PAIR ? 2 : static_cast<int>(S);
   const int cluster_id = static_cast<int>(blockIdx.x / csize);
   const int num_clusters = static_cast<int>(gridDim.x / csize);
@@ -489,11 +532,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
     ptx::tma_prefetch_desc(&tmap_b);
     for (int s = 0; s < S_; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], 1);
+      // B multicast: a stage is free once both CTAs' MMAs have read it
+      ptx::mbar_init(&empty_bar[s], Cfg::kMcB ? 2 : 1);
     }
     for (int b = 0; b < NBUF; ++b) {
       ptx::mbar_init(&tfull_bar[b], 1);
-      ptx::mbar_init(&tempty_bar[b], (PAIR ? 2 : 1) * Cfg::kEpiWarps);
+      ptx::mbar_init(&tempty_bar[b], (Cfg::kPairMma ? 2 : 1) * Cfg::kEpiWarps);
     }
     ptx::mbar_init(mma_done_bar, 1);
     ptx::mbar_init(staged_bar, Cfg::kEpiWarps);
@@ -503,7 +547,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
       ptx::mbar_init(&sf_empty_bar[j], 1);
     }
     if constexpr (Cfg::kFused) {
-      for (int j = 0; j < S_; ++j) ptx::mbar_init(&a8_ready_bar[j], 2);   // the two quantizer warps
+      for (int j = 0; j < S_; ++j) {
+        ptx::mbar_init(&a8_ready_bar[j], 2);   // the two quantizer warps
+        ptx::mbar_init(&xfull_bar[j], 1);
+      }
       for (int j = 0; j < Cfg::kSaSlots; ++j) {
         ptx::mbar_init(&sa_full_bar[j], 2);
         ptx::mbar_init(&sa_free_bar[j], Cfg::kEpiWarps);
@@ -512,7 +559,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
-    if constexpr (PAIR) {
+    if constexpr (Cfg::kPairMma) {
       ptx::tmem_alloc_pair<Cfg::kTmemAlloc>(tmem_slot);
       ptx::tmem_relinquish_pair();
     } else {
@@ -539,7 +586,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
   bool cluster_waited = !SPLIT;
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if constexpr (PAIR) {
+  if constexpr (Cfg::kPairMma) {
     // The pair's MMAs write the leader's TMEM address in both CTAs; make sure
     // both allocations returned it (both CTAs see the same answer).
     if (threadIdx.x == 0) {
@@ -549,9 +596,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
     }
     __syncthreads();
   }
-  const bool run_roles = !(PAIR && *pair_bad);
+  const bool run_roles = !(Cfg::kPairMma && *pair_bad);
   ptx::griddep_wait();  // the previous kernel's writes (our operands) are visible from here on
   ptx::griddep_launch();
+
 
   if (!run_roles) {
     // nothing: the CTA pair could not share its accumulators
@@ -574,16 +622,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
             ok = false;
             break;
           }
-          if constexpr (PAIR) {
+          if constexpr (Cfg::kMcB) {
+            // own 128 rows of A; half of B into both CTAs (each CTA's full
+            // barrier counts its A, its own half and the peer's half)
+            ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kABytes + Cfg::kBBytes);
+            ptx::tma_load_2d(smem_a + s * Cfg::kABytes, &tmap_a, &full_bar[s], kb * kBK, tm * TM + prank * kBM);
+            ptx::tma_load_2d_mc(smem_b + s * Cfg::kBBytes + prank * (BN / 2) * kBK, &tmap_b, &full_bar[s], kb * kBK,
+                                tn * BN + prank * (BN / 2), 0x3);
+          } else if constexpr (PAIR) {
             // both CTAs' loads count on the leader's barrier
             if (leader) ptx::mbar_arrive_expect_tx(&full_bar[s], 2 * Cfg::kStageBytes);
             const uint32_t fb = full0 + 8u * static_cast<uint32_t>(s);
             ptx::tma_load_2d_pair(smem_a + s * Cfg::kABytes, &tmap_a, fb, kb * kBK, tm * TM + prank * kBM);
             ptx::tma_load_2d_pair(smem_b + s * Cfg::kBBytes, &tmap_b, fb, kb * kBK, tn * BN + prank * (BN / 2));
           } else if constexpr (Cfg::kFused) {
-            // the activation in FP16/BF16 (FR rows, 128 columns = 256 bytes a row)
-            ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kXBytes + Cfg::kBBytes);
-            ptx::tma_load_2d(smem_x + s * Cfg::kXBytes, &tmap_a, &full_bar[s], kb * kBK, tm * kBM);
+            // the activation in FP16/BF16 (FR rows, 128 columns = 256 bytes a
+            // row) on a barrier of its own: the quantizer starts on it while
+            // the weight tile is still in flight
+            ptx::mbar_arrive_expect_tx(&xfull_bar[s], Cfg::kXBytes);
+            ptx::tma_load_2d(smem_x + s * Cfg::kXBytes, &tmap_a, &xfull_bar[s], kb * kBK, tm * kBM);
+            ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kBBytes);
             ptx::tma_load_2d(smem_b + s * Cfg::kBBytes, &tmap_b, &full_bar[s], kb * kBK, tn * BN);
           } else {
             ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kStageBytes);
@@ -601,12 +659,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
         const bool done = PAIR ? ptx::mbar_wait_bounded(&empty_bar[j % S_], (j / S_) & 1, p.timeout_ns)
                                : ptx::mbar_wait_bounded(&full_bar[j % S_], (j / S_) & 1, p.timeout_ns);
         if (!done) record_error(kErrProducer);
+        if (Cfg::kFused && !ptx::mbar_wait_bounded(&xfull_bar[j % S_], (j / S_) & 1, p.timeout_ns))
+          record_error(kErrProducer);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = Cfg::kUE8 ? ptx::idesc_mxf8_e4m3_ue8m0(TM, BN) : ptx::idesc_e4m3_f32(TM, BN);
+      // M of one MMA: 256 only for cta_group::2 pairs; B-multicast pairs
+      // issue single-CTA MMAs over their own 128 rows
+      constexpr int kMmaM = Cfg::kPairMma ? 2 * kBM : kBM;
+      constexpr uint32_t idesc =
+          Cfg::kUE8 ? ptx::idesc_mxf8_e4m3_ue8m0(kMmaM, BN) : ptx::idesc_e4m3_f32(kMmaM, BN);
       const uint32_t a0 = ptx::smem_u32(smem_a);
       const uint32_t b0 = ptx::smem_u32(smem_b);
       uint32_t consumed = 0, unit = 0;
@@ -617,8 +681,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           const bool new_unit = (MODE == kModeBlock) || i == 0;
           const uint32_t buf = unit % NBUF;
           if (new_unit) {
-            const bool freed = PAIR ? ptx::mbar_wait_cluster_bounded(&tempty_bar[buf], ((unit / NBUF) & 1) ^ 1, p.timeout_ns)
-                                    : ptx::mbar_wait_bounded(&tempty_bar[buf], ((unit / NBUF) & 1) ^ 1, p.timeout_ns);
+            const bool freed = Cfg::kPairMma
+                                   ? ptx::mbar_wait_cluster_bounded(&tempty_bar[buf], ((unit / NBUF) & 1) ^ 1, p.timeout_ns)
+                                   : ptx::mbar_wait_bounded(&tempty_bar[buf], ((unit / NBUF) & 1) ^ 1, p.timeout_ns);
             if (!freed) {
               record_error(kErrMma);
               ok = false;
@@ -658,7 +723,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           for (int k = 0; k < kBK / kMmaK; ++k) {
             // advance 32 bytes (2 x 16-byte units) along K inside the swizzled row
             const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (i > 0 || k > 0);
-            if constexpr (PAIR) ptx::mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
+            if constexpr (Cfg::kPairMma) ptx::mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
             else if constexpr (Cfg::kUE8)
               // byte i % 4 of every scale word belongs to this K block (A's
               // words in the slot's first four columns, B's after them)
@@ -666,7 +731,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
                                    sf_tmem + 4, acc);
             else ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
           }
-          if constexpr (PAIR) ptx::mma_commit_pair_mc(&empty_bar[s], 0x3);
+          if constexpr (Cfg::kPairMma) ptx::mma_commit_pair_mc(&empty_bar[s], 0x3);
+          else if constexpr (Cfg::kMcB) ptx::mma_commit_mc(&empty_bar[s], 0x3);   // both CTAs' copies of B are read
           else ptx::mma_commit(&empty_bar[s]);
           if constexpr (Cfg::kUE8) {
             if ((i & 3) == 3 || i == nkb - 1) {  // the group's last MMA: its scale slot frees when they complete
@@ -677,30 +743,32 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           ++consumed;
           const bool unit_done = (MODE == kModeBlock) || i == nkb - 1;
           if (unit_done) {
-            if constexpr (PAIR) ptx::mma_commit_pair_mc(&tfull_bar[buf], 0x3);
+            if constexpr (Cfg::kPairMma) ptx::mma_commit_pair_mc(&tfull_bar[buf], 0x3);
             else ptx::mma_commit(&tfull_bar[buf]);
             ++unit;
           }
         }
       }
       // Drain: all issued MMAs complete before TMEM can be released.
-      if constexpr (PAIR) ptx::mma_commit_pair_mc(mma_done_bar, 0x1);
+      if constexpr (Cfg::kPairMma) ptx::mma_commit_pair_mc(mma_done_bar, 0x1);
       else ptx::mma_commit(mma_done_bar);
       if (!ptx::mbar_wait_bounded(mma_done_bar, 0, p.timeout_ns)) record_error(kErrMma);
     }
   } else if (Cfg::kFused && (warp == 2 || warp == 3)) {
     // ------------------------------------ fused activation quantizer
-    // Per stage: the FR-row FP16/BF16 box of A has landed (full barrier).
-    // Each row of the box is one 1x128 token group ([P5] groups, [P2] s3
-    // steps 2-4): a half-warp reads its 256 bytes (8 elements a lane), takes
-    // the amax with four shuffles, s = fl32(amax / 448), and writes the
-    // E4M3 bytes into the stage's A tile in the MMA's 128-byte swizzled
-    // layout (16-byte unit u of row r at unit u ^ (r % 8)), and s into the
-    // slot of the scale ring that the epilogue reads for this K block.
-    // Warp 2 takes rows 0, 1, 4, 5, ..., warp 3 rows 2, 3, 6, 7, ...; rows
-    // past M are skipped (their bytes stay zero, their scales 1).
+    // Per stage: the FR-row FP16/BF16 box of A has landed (its own barrier;
+    // the weight tile may still be in flight).  Each row of the box is one
+    // 1x128 token group ([P5] groups, [P2] s3 steps 2-4): a half-warp reads
+    // its 256 bytes (8 elements a lane), the amax by shuffles, s =
+    // fl32(amax / 448), and the E4M3 bytes go into the stage's A tile in the
+    // MMA's 128-byte swizzled layout (16-byte unit u of row r at unit
+    // u ^ (r % 8)), s into the slot of the scale ring that the epilogue reads
+    // for this K block (quant_box16_rows, sixteen rows per call, one divide
+    // for all of them); warp 2 takes rows 0-15, 32-47, ..., warp 3 rows
+    // 16-31, 48-63, ...; rows past M are skipped (their bytes stay zero,
+    // their scales 1).
     if constexpr (Cfg::kFused) {
-      const int qwarp = warp - 2, half = lane >> 4, hl = lane & 15;
+      const int qwarp = warp - 2;
       uint32_t it = 0, u = 0;
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
@@ -714,7 +782,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           const uint32_t slot = u % Cfg::kSaSlots;
           bool got = true;
           if (lane == 0)
-            got = ptx::mbar_wait_bounded(&full_bar[s], (it / S_) & 1, p.timeout_ns) &&
+            got = ptx::mbar_wait_bounded(&xfull_bar[s], (it / S_) & 1, p.timeout_ns) &&
                   ptx::mbar_wait_bounded(&sa_free_bar[slot], ((u / Cfg::kSaSlots) & 1) ^ 1, p.timeout_ns);
           if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
             if (lane == 0) record_error(kErrProducer);
@@ -724,29 +792,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           const uint32_t xs = ptx::smem_u32(smem_x + s * Cfg::kXBytes);
           const uint32_t as = ptx::smem_u32(smem_a + s * Cfg::kABytes);
           float* sa_slot = sa_ring + slot * kBM;
-          for (int r0 = 2 * qwarp; r0 < FR; r0 += 4) {
-            if (tm * kBM + r0 >= p.M) break;  // warp-uniform: later rows are past M too
-            const int r = r0 + half;
-            const int m = tm * kBM + r;
-            const uint4 v = lds128(xs + static_cast<uint32_t>(r * 256 + hl * 16));
-            uint32_t a = amax_bits8(v);
-            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
-            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-            const UnitScale us(mag_to_float<DT>(a));
-            const uint2 q8 = quant8<DT>(v, us);
-            if (m < p.M) {
-              const uint32_t unit = static_cast<uint32_t>(hl >> 1) ^ static_cast<uint32_t>(r & 7);
-              const uint32_t dst = as + static_cast<uint32_t>(r * 128) + (unit << 4) + static_cast<uint32_t>((hl & 1) * 8);
-              asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(q8.x), "r"(q8.y) : "memory");
-              if (hl == 0) sa_slot[r] = us.s;
-              if (copy_out) {
-                reinterpret_cast<uint2*>(p.qa_out + static_cast<int64_t>(m) * p.K + kb * kBK)[hl] = q8;
-                if (hl == 0) p.sa_out[static_cast<int64_t>(kb) * p.M + m] = us.s;
-              }
-            }
-          }
+          const int mrem = p.M - tm * kBM;   // rows of this tile that exist
+          uint8_t* qo = copy_out ? p.qa_out + static_cast<int64_t>(tm * kBM) * p.K + kb * kBK : nullptr;
+          float* so = copy_out ? p.sa_out + static_cast<int64_t>(kb) * p.M + tm * kBM : nullptr;
+          for (int r0 = 16 * qwarp; r0 < FR && r0 < mrem; r0 += 32)
+            quant_box16_rows<DT>(xs, as, r0, mrem < FR ? mrem : FR, lane, sa_slot, qo, p.K, so);
           ptx::fence_proxy_async_shared();  // the E4M3 bytes, before the MMA reads them
           __syncwarp();
           if (lane == 0) {
@@ -756,25 +806,77 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
         }
       }
     }
-  } else if (warp == 3) {
-    // ----------------------------------------- UE8M0 scale-factor stager
-    // Per tile and group of four K blocks (in the tile's issue order): lane
-    // l builds the scale words of rows l, 32 + l, 64 + l, 96 + l of A's 128
-    // rows and of every 128 rows of B's BN (byte i = the code of the group's
-    // i-th K block; rows past M or N and K blocks past the tile's range get
-    // 127, i.e. 2^0), writes them as 16-byte rows of the slot's tiles and
-    // hands the slot to the MMA issuer.
+  } else if (Cfg::kUE8 && (warp == 2 || warp == 3)) {
+    // ----------------------------------------- UE8M0 scale-factor stagers
+    // Per tile and group of four K blocks (in the tile's issue order), warps
+    // 2 and 3 taking alternate groups: lane l builds the scale words of rows
+    // l, 32 + l, 64 + l, 96 + l of this CTA's 128 rows of A and of every 128
+    // rows of B's BN (byte i = the code of the group's i-th K block; rows
+    // past M or N and K blocks past the tile's range get 127, i.e. 2^0),
+    // writes them as 16-byte rows of the slot's tiles and hands the slot to
+    // the MMA issuer.  Every code load of a group is issued before any is
+    // used; a 128-row block of the weight has one code per K block, loaded
+    // once and shared by the warp.
     if constexpr (Cfg::kUE8) {
       const uint8_t* sa8 = reinterpret_cast<const uint8_t*>(p.sa);
       const uint8_t* sb8 = reinterpret_cast<const uint8_t*>(p.sb);
+      const uint32_t me = static_cast<uint32_t>(warp - 2);
       uint32_t sfg = 0;
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
         int tm, tn;
         tile_coords(t, p, tm, tn);
         const int rot = kb_rotation(tm, tn, nkb);
-        for (int g0 = 0; g0 < nkb; g0 += 4) {
+        for (int g0 = 0; g0 < nkb; g0 += 4, ++sfg) {
+          if ((sfg & 1u) != me) continue;   // the other stager's group
           const uint32_t slot = sfg % Cfg::kSfSlots;
+          int kbs[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = g0 + i;
+            kbs[i] = idx < nkb ? kb_begin + (idx + rot < nkb ? idx + rot : idx + rot - nkb) : -1;
+          }
+          const int m0 = tm * Cfg::kTileM + static_cast<int>(prank) * kBM + lane;
+          // Every load reads a valid address (K block and row clamped into
+          // range) and the out-of-range ones are replaced by 127 afterwards,
+          // so the loads carry no branches and all issue before any is used.
+          int kbc[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) kbc[i] = kbs[i] >= 0 ? kbs[i] : kb_begin;
+          // B: the weight block row of each 32-row chunk of the tile (a chunk
+          // never straddles a 128-row block; a 192-wide tile's 128-row scale
+          // tile can).  With BN a multiple of 128, or below 128, one block
+          // row serves a whole scale tile.
+          constexpr bool kOneBlockPerTile = BN % 128 == 0 || BN < 128;
+          constexpr int kBJ = kOneBlockPerTile ? 1 : 4;
+          uint32_t ca[4][4], cb[Cfg::kSfbTiles][kBJ][4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int m = min(m0 + 32 * j, p.M - 1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ca[j][i] = __ldg(sa8 + static_cast<int64_t>(kbc[i]) * p.M + m);
+          }
+#pragma unroll
+          for (int h = 0; h < Cfg::kSfbTiles; ++h)
+#pragma unroll
+            for (int jj = 0; jj < kBJ; ++jj) {
+              const int nb = min(tn * BN + h * 128 + jj * 32, p.N - 1) / 128;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) cb[h][jj][i] = __ldg(sb8 + static_cast<int64_t>(nb) * p.num_kb + kbc[i]);
+            }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (kbs[i] < 0) {   // K blocks past the tile's range: 2^0
+#pragma unroll
+              for (int j = 0; j < 4; ++j) ca[j][i] = 127u;
+#pragma unroll
+              for (int h = 0; h < Cfg::kSfbTiles; ++h)
+#pragma unroll
+                for (int jj = 0; jj < kBJ; ++jj) cb[h][jj][i] = 127u;
+            }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (m0 + 32 * j >= p.M) ca[j][0] = ca[j][1] = ca[j][2] = ca[j][3] = 127u;   // rows past M
           bool free_ok = true;
           if (lane == 0) free_ok = ptx::mbar_wait_bounded(&sf_empty_bar[slot], ((sfg / Cfg::kSfSlots) & 1) ^ 1,
                                                           p.timeout_ns);
@@ -783,50 +885,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
             ok = false;
             break;
           }
-          int kbs[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int idx = g0 + i;
-            kbs[i] = idx < nkb ? kb_begin + (idx + rot < nkb ? idx + rot : idx + rot - nkb) : -1;
-          }
           const uint32_t dst = ptx::smem_u32(sf_smem + slot * Cfg::kSfSlotBytes) + static_cast<uint32_t>(lane * 16);
-          {
-            uint32_t w[4];
+          uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int m = tm * kBM + j * 32 + lane;
-              uint32_t word = 0;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t c = (kbs[i] >= 0 && m < p.M) ? __ldg(sa8 + static_cast<int64_t>(kbs[i]) * p.M + m) : 127u;
-                word |= c << (8 * i);
-              }
-              w[j] = word;
-            }
-            ptx::sts128(dst, w[0], w[1], w[2], w[3]);
-          }
+          for (int j = 0; j < 4; ++j) w[j] = ca[j][0] | (ca[j][1] << 8) | (ca[j][2] << 16) | (ca[j][3] << 24);
+          ptx::sts128(dst, w[0], w[1], w[2], w[3]);
 #pragma unroll
           for (int h = 0; h < Cfg::kSfbTiles; ++h) {
-            uint32_t w[4];
+            // rows of this 128-row scale tile past N (or past the tile's BN) get 2^0
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+              const uint32_t* c = cb[h][kOneBlockPerTile ? 0 : j];
+              const uint32_t word = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
               const int n = tn * BN + h * 128 + j * 32 + lane;
-              const int64_t nb = n / 128;
-              uint32_t word = 0;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t c = (kbs[i] >= 0 && n < p.N && n < tn * BN + BN) ? __ldg(sb8 + nb * p.num_kb + kbs[i])
-                                                                                  : 127u;
-                word |= c << (8 * i);
-              }
-              w[j] = word;
+              w[j] = (n < p.N && h * 128 + j * 32 + lane < BN) ? word : 0x7F7F7F7Fu;
             }
             ptx::sts128(dst + 512 * (h + 1), w[0], w[1], w[2], w[3]);
           }
           ptx::fence_proxy_async_shared();  // these stores, before tcgen05.cp reads them
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&sf_full_bar[slot]);
-          ++sfg;
         }
       }
     }
@@ -854,6 +932,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
       int tm, tn;
       tile_coords(t, p, tm, tn);
       const int row = tm * TM + static_cast<int>(prank) * kBM + row_local;
+      // A warp whose 32 rows all lie past M (decode batches) skips the TMEM
+      // loads and the promotion; it still waits for and hands back every
+      // buffer, so the barrier phases stay in step.
+      const bool live = tm * TM + static_cast<int>(prank) * kBM + quarter * 32 < p.M;
       const int n_base = tn * BN + wg * CPT;
       uint16_t* crow = C + static_cast<int64_t>(row) * p.N;
 
@@ -886,12 +968,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           // (with one accumulator buffer, the next tile's MMAs wait for it),
           // then rounded and stored.
           uint32_t r[CPT];
+          if (live) {
 #pragma unroll
-          for (int c = 0; c < CPT / CW; ++c) tmem_load_nowait<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, &r[c * CW]);
-          ptx::tmem_ld_wait();
+            for (int c = 0; c < CPT / CW; ++c) tmem_load_nowait<CW>(tmem_base + lane_off + buf * BN + wg * CPT + c * CW, &r[c * CW]);
+            ptx::tmem_ld_wait();
+          }
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) release_tmem<PAIR>(&tempty_bar[buf]);
+          if (lane == 0) release_tmem<Cfg::kPairMma>(&tempty_bar[buf]);
           if (row < p.M) {
 #pragma unroll
             for (int c = 0; c < CPT / CW; ++c) {
@@ -914,14 +998,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) release_tmem<PAIR>(&tempty_bar[buf]);
+        if (lane == 0) release_tmem<Cfg::kPairMma>(&tempty_bar[buf]);
         ++unit;
         if (!ok) break;
       } else {
         constexpr int KBT = Cfg::kBatch;
-        float acc[CPT];
+        float2 acc2[CPT / 2];
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < CPT / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
         // weight block row of this warpgroup's columns (clamped: a slice past
         // the last column of a ragged tile is computed but never stored)
         const int nb = (n_base < p.N ? n_base : p.N - 1) / 128;
@@ -938,12 +1022,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           const int kb_stop = kb_begin + nkb;
           const uint32_t taddr0 = tmem_base + lane_off + static_cast<uint32_t>(wg * CPT);
           int kb = kb_begin + rot;
-          float sa_c = __ldg(sa_col + kb * sa_step), sb_c = __ldg(sb_row + kb);
+          float sa_c = Cfg::kFused ? 0.0f : __ldg(sa_col + kb * sa_step), sb_c = __ldg(sb_row + kb);
           for (int i = 0; i < nkb; ++i) {
-            const float sc = sa_c * sb_c;
+            float sc = sa_c * sb_c;
+            const float sb_now = sb_c;
             const int kn = kb + 1 == kb_stop ? kb_begin : kb + 1;
             if (i + 1 < nkb) {
-              sa_c = __ldg(sa_col + kn * sa_step);
+              if constexpr (!Cfg::kFused) sa_c = __ldg(sa_col + kn * sa_step);
               sb_c = __ldg(sb_row + kn);
             }
             kb = kn;
@@ -953,8 +1038,30 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
               ok = false;
               break;
             }
+            if constexpr (Cfg::kFused) {
+              // this K block's token scale, from the quantizer's ring
+              const uint32_t slot = unit % Cfg::kSaSlots;
+              bool got = true;
+              if (lane == 0) got = ptx::mbar_wait_bounded(&sa_full_bar[slot], (unit / Cfg::kSaSlots) & 1, p.timeout_ns);
+              if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
+                if (lane == 0) record_error(kErrEpilogue);
+                ok = false;
+                break;
+              }
+              __syncwarp();  // lane 0's acquire orders the other lanes' reads too
+              sc = sa_ring[slot * kBM + row_local] * sb_now;
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(&sa_free_bar[slot]);
+            }
             ptx::tc_fence_after();
             const uint32_t taddr = taddr0 + buf * BN;
+            if (!live) {
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) release_tmem<Cfg::kPairMma>(&tempty_bar[buf]);
+              unit += 1;
+              continue;
+            }
 #pragma unroll
             for (int c0 = 0; c0 < CPT; c0 += LC) {
               uint32_t part[LC];
@@ -964,10 +1071,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
               if (c0 + LC == CPT) {
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) release_tmem<PAIR>(&tempty_bar[buf]);
+                if (lane == 0) release_tmem<Cfg::kPairMma>(&tempty_bar[buf]);
               }
 #pragma unroll
-              for (int j = 0; j < LC; j += 2) promote2(&acc[c0 + j], part[j], part[j + 1], sc);
+              for (int j = 0; j < LC; j += 2) promote2(acc2[(c0 + j) / 2], part[j], part[j + 1], make_float2(sc, sc));
             }
             unit += 1;
           }
@@ -1022,7 +1129,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
           }
           if (!ok) break;
           ptx::tc_fence_after();
-          {
+          if (!live) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+              for (int j = 0; j < nbat; ++j) release_tmem<Cfg::kPairMma>(&tempty_bar[(unit + j) % NBUF]);
+            unit += nbat;
+          } else {
             uint32_t part[KBT][CPT];
 #pragma unroll
             for (int j = 0; j < KBT; ++j) {
@@ -1037,20 +1150,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
-              for (int j = 0; j < nbat; ++j) release_tmem<PAIR>(&tempty_bar[(unit + j) % NBUF]);
+              for (int j = 0; j < nbat; ++j) release_tmem<Cfg::kPairMma>(&tempty_bar[(unit + j) % NBUF]);
             unit += nbat;
 #pragma unroll
             for (int j = 0; j < KBT; ++j)
               if (j < nbat) {
 #pragma unroll
-                for (int c = 0; c < CPT; c += 2) promote2(&acc[c], part[j][c], part[j][c + 1], sc[j]);
+                for (int c = 0; c < CPT; c += 2) promote2(acc2[c / 2], part[j][c], part[j][c + 1], make_float2(sc[j], sc[j]));
               }
           }
         }
         }
         if (!ok) break;
         if constexpr (SPLIT) {
-          if (row_local < split_rows(p, tm, static_cast<int>(S)) * static_cast<int>(S)) stage_row<CPT>(srow, acc);
+          if (row_local < split_rows(p, tm, static_cast<int>(S)) * static_cast<int>(S)) stage_row2<CPT>(srow, acc2);
           if (!cluster_waited) {  // peers' barriers are initialised from here on
             ptx::cluster_wait();
             cluster_waited = true;
@@ -1062,7 +1175,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
         } else {
           if (row < p.M) {
 #pragma unroll
-            for (int c = 0; c < CPT / CW; ++c) store_row<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, acc + c * CW);
+            for (int c = 0; c < CPT / CW; ++c) store_row2<OUT, CW>(crow, n_base + c * CW, p.N, vec_ok, acc2 + c * CW / 2);
           }
         }
       }
@@ -1077,7 +1190,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, SPLIT, PAIR, FR>::kThreads, 
   if constexpr (PAIR) ptx::cluster_sync_all();
   if (warp == 2) {
     ptx::tc_fence_after();
-    if constexpr (PAIR) ptx::tmem_dealloc_pair<Cfg::kTmemAlloc>(tmem_base);
+    if constexpr (Cfg::kPairMma) ptx::tmem_dealloc_pair<Cfg::kTmemAlloc>(tmem_base);
     else ptx::tmem_dealloc<Cfg::kTmemAlloc>(tmem_base);
   }
   if constexpr (SPLIT || PAIR) ptx::cluster_sync_all();  // no CTA leaves while a peer may touch its shared memory

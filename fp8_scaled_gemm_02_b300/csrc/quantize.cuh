@@ -224,6 +224,70 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// The fused linear's activation quantizer for one warp: rows [r0, r0 + 16)
+// of an FP16/BF16 box in shared memory (256-byte rows at xs; rows at or past
+// `rows` are not read) become 1x128 token groups.  Half a warp holds a row
+// (16-byte loads, eight rows a half), the amax is reduced by shuffles on
+// pairs of rows packed into one word, lane l (< 16) computes the scale and
+// reciprocal of row r0 + l (one divide and one reciprocal for all sixteen
+// rows), and the half-warps take their rows' s and y back by shuffle; the
+// elements then follow the quantizers' division path (bit-identical).  The
+// E4M3 bytes go to the MMA's 128-byte swizzled tile at as (16-byte unit u of
+// row r at u ^ (r % 8)), s to sa_rows[r]; if qo is set, also the bytes to
+// qo + r * qld and s to so[r].
+template <int DT>
+__device__ __forceinline__ void quant_box16_rows(uint32_t xs, uint32_t as, int r0, int rows, int lane, float* sa_rows,
+                                                 uint8_t* qo, int64_t qld, float* so) {
+  const int half = lane >> 4, hl = lane & 15;
+  uint4 v[8];
+  uint32_t a[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r = r0 + 2 * q + half;
+    v[q] = r < rows ? lds128(xs + static_cast<uint32_t>(r * 256 + hl * 16)) : make_uint4(0u, 0u, 0u, 0u);
+    a[q] = amax_bits8(v[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < 8; q += 2) {
+    uint32_t pk = a[q] | (a[q + 1] << 16);   // magnitudes are 15-bit: two per word
+#pragma unroll
+    for (int d = 8; d >= 1; d >>= 1) pk = __vmaxu2(pk, __shfl_xor_sync(0xFFFFFFFFu, pk, d));
+    a[q] = pk & 0xFFFFu;
+    a[q + 1] = pk >> 16;
+  }
+  uint32_t mine = 0;   // lane l < 16: the amax of row r0 + l (row 2q + h sits in half h)
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t t = __shfl_sync(0xFFFFFFFFu, a[q], (lane & 1) << 4);
+    if ((lane >> 1) == q) mine = t;
+  }
+  const UnitScale own(mag_to_float<DT>(mine));
+  uint2 q8[8];
+  float sq[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float s = __shfl_sync(0xFFFFFFFFu, own.s, 2 * q + half);
+    const float y = __shfl_sync(0xFFFFFFFFu, own.y, 2 * q + half);
+    const UnitScale us(s, y, !(s >= 0x1p-90f));   // as UnitScale(amax) computes them
+    q8[q] = quant8<DT>(v[q], us);
+    sq[q] = s;
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r = r0 + 2 * q + half;
+    if (r < rows) {
+      const uint32_t unit = static_cast<uint32_t>(hl >> 1) ^ static_cast<uint32_t>(r & 7);
+      const uint32_t dst = as + static_cast<uint32_t>(r * 128) + (unit << 4) + static_cast<uint32_t>((hl & 1) * 8);
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(q8[q].x), "r"(q8[q].y) : "memory");
+      if (hl == 0) sa_rows[r] = sq[q];
+      if (qo != nullptr) {
+        reinterpret_cast<uint2*>(qo + static_cast<int64_t>(r) * qld)[hl] = q8[q];
+        if (hl == 0) so[r] = sq[q];
+      }
+    }
+  }
+}
+
 // 16-byte load that does not allocate in L1 and asks L2 to keep the line
 // (evict-last policy `pol`, from createpolicy): for data read again soon.
 __device__ __forceinline__ uint4 ld_keep_l2(const uint4* p, uint64_t pol) {

@@ -269,8 +269,12 @@ FP8S_API fp8s_status fp8_e5m2_decode(const uint8_t* q, int64_t numel, void* y, f
  *       receive the quantized activation and its scales (byte- and
  *       bit-identical to fp8_quantize_token_group's).
  * Designed for decode batches (M <= 128; M <= 16 uses a 16-row activation
- * box), where the weight stream dominates; any M is correct.  Tile
- * overrides (fp8s_gemm_override) apply with bn 64 or 128 and no pair.
+ * box), where the weight stream dominates; any M is correct, but above 16
+ * rows every CTA of a row of output tiles repeats the quantization of its
+ * activation tile, so the two-call path (fp8_quantize_token_group, then
+ * fp8_gemm_scaled) is faster there.  Tile overrides (fp8s_gemm_override)
+ * apply with bn 64 or 128 (any split), or bn 192 (split only for M <= 16),
+ * and no pair; others give FP8S_ERR_SHAPE.
  * All pointers 16-byte aligned.  One kernel launch.
  */
 FP8S_API fp8s_status fp8_linear_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K, const uint8_t* qw,

@@ -178,7 +178,7 @@ def test_default_lines_end_with_the_headline():
 
     lines = bench.lines_of(Args())
     assert [(a.workload, a.modes) for a in lines][-1] == ("outlier_16384x8192x8192", "")
-    assert ("llama2_7b_m1", "block,fused") in [(a.workload, a.modes) for a in lines]
+    assert ("llama2_7b_m1", "block_fp8w,fused_fp8w") in [(a.workload, a.modes) for a in lines]
     Args.workload = "llama2_7b_m8"
     assert [(a.workload, a.modes) for a in bench.lines_of(Args())] == [("llama2_7b_m8", "")]
 
@@ -197,3 +197,19 @@ def test_fused_and_ue8m0_plans():
     fused = [ks for lin, mode, ks in plan if lin.name == "o" and mode == "fused"][0]
     M, N, K = 1, 4096, 4096
     assert fused[1][2] == M * K * 2 + N * K + 4 * 32 * 32 + 2 * M * N and fused[1][3] == 2 * M * N * K
+
+
+def test_fp8_weight_plans():
+    """Weights held in FP8: a step is the activation quantize + GEMM, or the
+    fused linear alone; no weight quantization in the step."""
+    import bench
+
+    class Args:
+        workload = "llama2_7b_m1"
+        modes = "block_fp8w,fused_fp8w"
+
+    plan = bench.kernel_plan(bench.workload_of(Args()))
+    for lin, mode, ks in plan:
+        names = [k[0] for k in ks]
+        assert "quant_weight_block" not in names
+        assert names == (["quant_token_group", "gemm_block"] if mode == "block_fp8w" else ["linear_fused"])

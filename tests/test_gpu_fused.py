@@ -83,7 +83,7 @@ def test_fused_distinct_group_magnitudes(M):
     run_fused(a, w, "bf16")
 
 
-@pytest.mark.parametrize("bn,splits", [(64, 1), (128, 1), (64, 2), (128, 4), (128, 8), (64, 8)])
+@pytest.mark.parametrize("bn,splits", [(64, 1), (128, 1), (192, 1), (64, 2), (128, 4), (128, 8), (64, 8)])
 @pytest.mark.parametrize("M", [5, 128])
 def test_fused_every_tile(bn, splits, M):
     a, w = _distinct(M, 520, 1024, seed=84)
@@ -99,3 +99,28 @@ def test_fused_llama_decode(m):
     wl = synth.WORKLOADS[f"llama2_7b_m{m}"]
     for lin in wl.linears:
         run_fused(synth.activation(wl, lin), synth.weight(wl, lin), "bf16")
+
+
+def test_fused_refuses_unbuilt_tiles():
+    """192-wide tiles split K only for M <= 16; 256- and 32-wide tiles do not exist."""
+    w = synth.random_bits((520, 1024), "bf16", seed=85, tensor_id=2, std=0.02)
+    qw, sw = F.fp8_quantize_weight_block(to_dev(w, "bf16"))
+    for M, bn, splits in [(20, 192, 2), (4, 256, 1), (4, 32, 1)]:
+        a = synth.random_bits((M, 1024), "bf16", seed=85, tensor_id=1)
+        F.fp8s_gemm_override(bn, splits)
+        try:
+            with pytest.raises(F.Fp8sError):
+                F.fp8_linear_token_group(to_dev(a, "bf16"), qw, sw)
+        finally:
+            F.fp8s_gemm_override(0)
+
+
+@pytest.mark.parametrize("splits", [2, 4, 8])
+def test_fused_192_split_small_m(splits):
+    """192-wide tiles with split-K (16-row activation boxes, M <= 16)."""
+    a, w = _distinct(7, 700, 1024, seed=86)
+    F.fp8s_gemm_override(192, splits)
+    try:
+        run_fused(a, w, "bf16")
+    finally:
+        F.fp8s_gemm_override(0)

@@ -169,6 +169,20 @@ def test_gemm_every_tile(bn, splits):
         F.fp8s_gemm_override(0)
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 520, 1024), (600, 1000, 2048)])
+def test_gemm_multicast_pairs(M, N, K):
+    """Two CTAs of a cluster on a 256-row tile, each loading half of the
+    256-wide weight tile by TMA multicast into both; the scale factors stay
+    per CTA (an odd number of 128-row tiles leaves a pair's second CTA
+    past M)."""
+    a, w = _distinct(M, N, K, seed=67 + M)
+    F.fp8s_gemm_override(256, 1, True)
+    try:
+        run_ue8_linear(a, w, "bf16", "bf16")
+    finally:
+        F.fp8s_gemm_override(0)
+
+
 def _sample_rows(M, n=32, seed=0):
     rng = np.random.default_rng(seed)
     return np.unique(np.concatenate([[0, M - 1], rng.choice(M, size=min(n, M), replace=False)]))
