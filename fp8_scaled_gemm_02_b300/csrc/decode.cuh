@@ -18,8 +18,8 @@
 //               swizzle, a STAGES-deep ring.
 //   warp 1      MMA issuer: tcgen05.mma kind::f8f6f4, M = 128, N = MT, four
 //               per K block, a fresh TMEM buffer per K block.
-//   warp 2      TMEM allocation; fused: warps 2 and 3 quantize the activation
-//               (warp 2 the even stages of the ring, warp 3 the odd ones;
+//   warp 2      TMEM allocation; fused: warps 2-3 and 8-11 quantize the
+//               activation (stage s of the ring belongs to quantizer s % 6;
 //               each row of the box is a 1x128 token group, quantized into
 //               the stage's swizzled E4M3 tile, its scale into a ring the
 //               epilogue reads).
@@ -33,9 +33,11 @@
 // transposed: for a fixed token the 32 lanes of a warp write 32 consecutive
 // columns.
 //
-// Shared memory stays near 100 KB and TMEM at MT * 8 columns, so two CTAs fit
-// on an SM and a grid of up to two CTAs per SM is resident at once.  Every
-// wait is bounded as in gemm.cuh.
+// A kernel that holds tensor-memory instructions is resident at one CTA per
+// SM (the occupancy the CUDA runtime reports for it, whatever its registers
+// and shared memory), so each CTA takes a ring of ~200 KB, deep enough to
+// keep an SM's share of the HBM bandwidth in flight.  Every wait is bounded
+// as in gemm.cuh.
 #pragma once
 
 #include "gemm.cuh"
@@ -46,27 +48,45 @@ template <int MT, bool SPLIT, bool FUSED>
 struct DecCfg {
   static_assert(MT == 16 || MT == 32, "token columns per MMA");
   static constexpr int kEpiWarps = 4;
-  static constexpr int kThreads = 128 + 32 * kEpiWarps;
+  // Two CTAs per SM (~100 KB of shared memory, <= 128 registers) for the
+  // unfused kernel and the fused MT = 16 one; the fused MT = 32 kernel takes
+  // an SM alone.  Fused: kQWarps quantizer warps, 2-3 and 8.. (the epilogue
+  // keeps warps 4-7, whose warp index modulo 4 is their TMEM lane quarter).
+  static constexpr int kCtasPerSm = (FUSED && MT == 32) ? 1 : 2;
+  static constexpr int kQWarps = FUSED ? (MT == 16 ? 2 : 4) : 0;
+  static constexpr int kThreads = 128 + 32 * kEpiWarps + (FUSED ? 32 * (kQWarps - 2) : 0);
   static constexpr int kWBytes = kBM * kBK;                 // 128 weight rows x one K block
   static constexpr int kXBytes = MT * kBK;                  // E4M3 activation rows
-  static constexpr int kX16Bytes = FUSED ? MT * kBK * 2 : 0;  // fused: FP16/BF16 activation box (M <= MT rows)
-  static constexpr int kStageBytes = kWBytes + kXBytes + kX16Bytes;
+  // Unfused: a stage holds the weight tile and the E4M3 activation tile.
+  // Fused: the stage holds the weight tile only; the activation has a ring of
+  // its own, kXSlots slots of [FP16/BF16 box (MT x 256 B) | E4M3 tile
+  // (MT x 128 B)], slot j owned by quantizer j % kQWarps.
+  static constexpr int kStageBytes = FUSED ? kWBytes : kWBytes + kXBytes;
+  static constexpr int kXSlots = 2 * kQWarps;
+  static constexpr int kX16Bytes = MT * kBK * 2;
+  static constexpr int kXSlotBytes = FUSED ? kX16Bytes + kXBytes : 0;
+  static constexpr int kXRingBytes = kXSlots * kXSlotBytes;
   static constexpr int kPitch = MT + 4;                     // staging row pitch (floats): 16-byte rows
   static constexpr int kStagingBytes = kBM * kPitch * 4;
   static constexpr int kRecvBytes = SPLIT ? 112 * kPitch * 4 : 0;
-  static constexpr int kSaSlots = FUSED ? 8 : 0;            // fused: token scales per K block
+  static constexpr int kSaSlots = FUSED ? 12 : 0;           // fused: token scales per K block
   static constexpr int kSaBytes = kSaSlots * MT * 4;
-  static constexpr int kBudget = 104 * 1024;               // two CTAs per SM
-  static constexpr int kStagesRaw = (kBudget - kRecvBytes - kSaBytes - 1024) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kBudget = kCtasPerSm == 2 ? 104 * 1024 : 220 * 1024;
+  static constexpr int kStagesRaw = (kBudget - kXRingBytes - kRecvBytes - kSaBytes - 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(!SPLIT || kStages * kStageBytes >= kStagingBytes, "staging fits in the ring");
   static constexpr int kNBuf = 8;
   static constexpr int kTmemCols = kNBuf * MT;               // 128 or 256: a power of two
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 3 + (FUSED ? 2 * kStages + 2 * kSaSlots : 0)) + 16;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRecvBytes + kSaBytes + kBarBytes;
-  static_assert(kSmemBytes <= 113 * 1024, "shared memory: two CTAs per SM");
-  static constexpr int kCtasPerSm = 2;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 3 + (FUSED ? 3 * kXSlots + 2 * kSaSlots : 0)) + 16;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kXRingBytes + kRecvBytes + kSaBytes + kBarBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  // A quantizer runs at most kXSlots K blocks ahead of the MMA, which runs at
+  // most kNBuf ahead of the epilogue; with 2 * kSaSlots above that lead no
+  // wait on a scale slot is two phases behind.  Slot j of either ring is
+  // always used by quantizer j % kQWarps.
+  static_assert(kSaSlots == 0 || 2 * kSaSlots > kXSlots + kNBuf, "scale slots");
+  static_assert(kSaSlots % (kQWarps > 0 ? kQWarps : 1) == 0, "scale slots per quantizer");
 };
 
 // Sums this CTA's R weight rows over the S partials in rank order and stores
@@ -98,7 +118,7 @@ __device__ __forceinline__ void dec_reduce(const float* send, const float* recv,
 }
 
 template <int MT, int OUT, bool SPLIT, bool FUSED>
-__global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <= 128 registers
+__global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT, SPLIT, FUSED>::kCtasPerSm)
     fp8_decode_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                       const GemmParams p) {
   using Cfg = DecCfg<MT, SPLIT, FUSED>;
@@ -108,12 +128,13 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <=
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int XS = Cfg::kXSlots > 0 ? Cfg::kXSlots : 1;   // (unfused: no activation slots)
   uint8_t* w_ring = smem;
-  uint8_t* x_ring = w_ring + S_ * Cfg::kWBytes;
-  uint8_t* x16_ring = x_ring + S_ * Cfg::kXBytes;
+  uint8_t* x_ring = w_ring + S_ * Cfg::kWBytes;             // unfused: E4M3 tiles, one per stage
+  uint8_t* xq_ring = smem + S_ * Cfg::kStageBytes;          // fused: activation slots
   float* staging = reinterpret_cast<float*>(smem);  // split-K: after the ring has drained
-  const float* recv = reinterpret_cast<const float*>(smem + S_ * Cfg::kStageBytes);
-  float* sa_ring = reinterpret_cast<float*>(smem + S_ * Cfg::kStageBytes + Cfg::kRecvBytes);
+  const float* recv = reinterpret_cast<const float*>(xq_ring + Cfg::kXRingBytes);
+  float* sa_ring = reinterpret_cast<float*>(xq_ring + Cfg::kXRingBytes + Cfg::kRecvBytes);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sa_ring) + Cfg::kSaBytes);
   uint64_t* empty_bar = full_bar + S_;
   uint64_t* tfull_bar = empty_bar + S_;
@@ -121,9 +142,10 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <=
   uint64_t* mma_done_bar = tempty_bar + NBUF;
   uint64_t* staged_bar = mma_done_bar + 1;
   uint64_t* recv_bar = staged_bar + 1;
-  uint64_t* x8_ready_bar = recv_bar + 1;                          // fused: stage's E4M3 rows written
-  uint64_t* xfull_bar = x8_ready_bar + (FUSED ? S_ : 0);          // fused: stage's activation box landed
-  uint64_t* sa_full_bar = xfull_bar + (FUSED ? S_ : 0);           // fused: a scale slot written
+  uint64_t* x8_ready_bar = recv_bar + 1;                          // fused: slot's E4M3 rows written
+  uint64_t* xfull_bar = x8_ready_bar + (FUSED ? XS : 0);          // fused: slot's activation box landed
+  uint64_t* xempty_bar = xfull_bar + (FUSED ? XS : 0);            // fused: slot's MMAs done
+  uint64_t* sa_full_bar = xempty_bar + (FUSED ? XS : 0);          // fused: a scale slot written
   uint64_t* sa_free_bar = sa_full_bar + Cfg::kSaSlots;            // fused: a scale slot read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sa_free_bar + Cfg::kSaSlots);
 
@@ -156,9 +178,10 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <=
     ptx::mbar_init(staged_bar, Cfg::kEpiWarps);
     ptx::mbar_init(recv_bar, 1);
     if constexpr (FUSED) {
-      for (int s = 0; s < S_; ++s) {
-        ptx::mbar_init(&x8_ready_bar[s], 1);   // the quantizer warp of that use of the stage
-        ptx::mbar_init(&xfull_bar[s], 1);
+      for (int j = 0; j < XS; ++j) {
+        ptx::mbar_init(&x8_ready_bar[j], 1);   // the slot's quantizer warp
+        ptx::mbar_init(&xfull_bar[j], 1);
+        ptx::mbar_init(&xempty_bar[j], 1);     // the MMA issuer's commit
       }
       for (int j = 0; j < Cfg::kSaSlots; ++j) {
         ptx::mbar_init(&sa_full_bar[j], 1);
@@ -174,8 +197,11 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <=
   if constexpr (FUSED) {
     // activation rows past M are never written by the quantizer: they stay
     // zero, and their token scales 0 (the products they meet are zero)
-    for (int i = threadIdx.x; i < S_ * Cfg::kXBytes / 16; i += Cfg::kThreads)
-      ptx::sts128(ptx::smem_u32(x_ring) + 16u * static_cast<uint32_t>(i), 0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < XS * Cfg::kXBytes / 16; i += Cfg::kThreads) {
+      const int j = i / (Cfg::kXBytes / 16), u = i - j * (Cfg::kXBytes / 16);
+      ptx::sts128(ptx::smem_u32(xq_ring + j * Cfg::kXSlotBytes + Cfg::kX16Bytes) + 16u * static_cast<uint32_t>(u), 0u,
+                  0u, 0u, 0u);
+    }
     for (int i = threadIdx.x; i < Cfg::kSaSlots * MT; i += Cfg::kThreads) sa_ring[i] = 0.0f;
     ptx::fence_proxy_async_shared();
   }
@@ -202,9 +228,7 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <=
           break;
         }
         if constexpr (FUSED) {
-          ptx::mbar_arrive_expect_tx(&xfull_bar[s], x16_box_bytes);
-          ptx::tma_load_2d(x16_ring + s * Cfg::kX16Bytes, &tmap_x, &xfull_bar[s], kb * kBK, 0);
-          ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes);
+          ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes);   // the activation: the quantizers' loads
         } else {
           ptx::mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes + Cfg::kXBytes);
           ptx::tma_load_2d(x_ring + s * Cfg::kXBytes, &tmap_x, &full_bar[s], kb * kBK, 0);
@@ -213,77 +237,105 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, 2)   // <=
         ++issued;
       }
       // every issued load lands before the CTA may exit
-      for (int j = issued > S_ ? issued - S_ : 0; j < issued; ++j) {
+      for (int j = issued > S_ ? issued - S_ : 0; j < issued; ++j)
         if (!ptx::mbar_wait_bounded(&full_bar[j % S_], (j / S_) & 1, p.timeout_ns)) record_error(kErrProducer);
-        if (FUSED && !ptx::mbar_wait_bounded(&xfull_bar[j % S_], (j / S_) & 1, p.timeout_ns))
-          record_error(kErrProducer);
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBM, MT);
-      const uint32_t w0 = ptx::smem_u32(w_ring), x0 = ptx::smem_u32(x_ring);
+      const uint32_t w0 = ptx::smem_u32(w_ring), x0 = ptx::smem_u32(x_ring), xq0 = ptx::smem_u32(xq_ring);
       for (int i = 0; i < nkb; ++i) {
         const int buf = i % NBUF, s = i % S_;
+        const int xj = FUSED ? i % XS : 0;
         if (!ptx::mbar_wait_bounded(&tempty_bar[buf], ((i / NBUF) & 1) ^ 1, p.timeout_ns) ||
             !ptx::mbar_wait_bounded(&full_bar[s], (i / S_) & 1, p.timeout_ns) ||
-            (FUSED && !ptx::mbar_wait_bounded(&x8_ready_bar[s], (i / S_) & 1, p.timeout_ns))) {
+            (FUSED && !ptx::mbar_wait_bounded(&x8_ready_bar[xj], (i / XS) & 1, p.timeout_ns))) {
           record_error(kErrMma);
           break;
         }
         ptx::tc_fence_after();
         const uint64_t adesc = ptx::smem_desc_sw128_kmajor(w0 + s * Cfg::kWBytes);
-        const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(x0 + s * Cfg::kXBytes);
+        const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(
+            FUSED ? xq0 + static_cast<uint32_t>(xj * Cfg::kXSlotBytes + Cfg::kX16Bytes) : x0 + s * Cfg::kXBytes);
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * MT);
 #pragma unroll
         for (int k = 0; k < kBK / kMmaK; ++k) ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
         ptx::mma_commit(&empty_bar[s]);
+        if constexpr (FUSED) ptx::mma_commit(&xempty_bar[xj]);
         ptx::mma_commit(&tfull_bar[buf]);
       }
       ptx::mma_commit(mma_done_bar);
       if (!ptx::mbar_wait_bounded(mma_done_bar, 0, p.timeout_ns)) record_error(kErrMma);
     }
-  } else if (FUSED && (warp == 2 || warp == 3)) {
+  } else if (FUSED && (warp == 2 || warp == 3 || warp >= 8)) {
     // --------------------------------------- fused activation quantizer
-    // Per stage: the M-row box of x has landed (the weight tile may still be
-    // in flight).  Each row is one 1x128 token group ([P5] groups, [P2] s3
-    // steps 2-4), quantized by quant_box16_rows sixteen rows at a time into
-    // the stage's swizzled E4M3 tile, its scale into the ring slot of this K
-    // block.  Each stage of the ring belongs to one warp (warp 2 the even
-    // stages, warp 3 the odd ones), so every barrier of a stage sees its
-    // phases waited for and arrived on in order by one warp.
+    // K block i (in the CTA's issue order) goes to quantizer i % kQWarps and
+    // activation slot j = i % kXSlots (two slots per quantizer).  A slot's
+    // FP16/BF16 box is free again once its quantizer has read it, so the
+    // quantizer reloads it (TMA) for K block i + kXSlots right after
+    // quantizing K block i: the boxes run two K blocks of this quantizer
+    // ahead.  The slot's E4M3 tile is free once the MMA of K block
+    // i - kXSlots has committed.  Each row of a box is one 1x128 token group
+    // ([P5] groups, [P2] s3 steps 2-4), quantized by quant_box16_rows sixteen
+    // rows at a time into the slot's swizzled E4M3 tile, its scale into the
+    // scale-ring slot of this K block.  Every barrier of a slot is waited
+    // for and arrived on by its one quantizer, in order.
     if constexpr (FUSED) {
-      const int qwarp = warp - 2;
+      const int qwarp = warp < 4 ? warp - 2 : warp - 6;   // 0 .. kQWarps - 1
+      constexpr int NQ = Cfg::kQWarps;
       const bool copy_out = p.qa_out != nullptr && tn == 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % S_;
-        if ((s & 1) != qwarp) continue;
-        const int kb = kb_at(i);
+      auto load_box = [&](int k) {   // lane 0: the box of K block k into its slot (the slot's box is free)
+        const int j = k % XS;
+        ptx::mbar_arrive_expect_tx(&xfull_bar[j], x16_box_bytes);
+        ptx::tma_load_2d(xq_ring + j * Cfg::kXSlotBytes, &tmap_x, &xfull_bar[j], kb_at(k) * kBK, 0);
+      };
+      int next_issue = qwarp, next_wait = qwarp;   // lane 0's bookkeeping of this quantizer's loads
+      if (lane == 0)
+        for (; next_issue < nkb && next_issue < qwarp + XS; next_issue += NQ) load_box(next_issue);
+      bool ok = true;
+      for (int i = qwarp; i < nkb; i += NQ) {
+        const int j = i % XS;
         const int slot = i % Cfg::kSaSlots;
         bool got = true;
-        if (lane == 0)
-          got = ptx::mbar_wait_bounded(&xfull_bar[s], (i / S_) & 1, p.timeout_ns) &&
+        if (lane == 0) {
+          got = ptx::mbar_wait_bounded(&xfull_bar[j], (i / XS) & 1, p.timeout_ns);
+          if (got) next_wait = i + NQ;
+          got = got && ptx::mbar_wait_bounded(&xempty_bar[j], ((i / XS) & 1) ^ 1, p.timeout_ns) &&
                 ptx::mbar_wait_bounded(&sa_free_bar[slot], ((i / Cfg::kSaSlots) & 1) ^ 1, p.timeout_ns);
+        }
         if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
           if (lane == 0) record_error(kErrProducer);
+          ok = false;
           break;
         }
-        const uint32_t xs = ptx::smem_u32(x16_ring + s * Cfg::kX16Bytes);
-        const uint32_t as = ptx::smem_u32(x_ring + s * Cfg::kXBytes);
+        const int kb = kb_at(i);
+        const uint32_t xs = ptx::smem_u32(xq_ring + j * Cfg::kXSlotBytes);
+        const uint32_t as = xs + static_cast<uint32_t>(Cfg::kX16Bytes);
         uint8_t* qo = copy_out ? p.qa_out + static_cast<int64_t>(kb) * kBK : nullptr;
         float* so = copy_out ? p.sa_out + static_cast<int64_t>(kb) * p.M : nullptr;
         for (int r0 = 0; r0 < MT && r0 < p.M; r0 += 16)
           quant_box16_rows<DT>(xs, as, r0, p.M, lane, sa_ring + slot * MT, qo, p.K, so);
-        ptx::fence_proxy_async_shared();  // the E4M3 bytes, before the MMA reads them
+        // the E4M3 bytes before the MMA reads them, and this warp's reads of
+        // the box before the next TMA write into it
+        ptx::fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-          ptx::mbar_arrive(&x8_ready_bar[s]);
+          ptx::mbar_arrive(&x8_ready_bar[j]);
           ptx::mbar_arrive(&sa_full_bar[slot]);
+          if (next_issue < nkb) {
+            load_box(next_issue);
+            next_issue += NQ;
+          }
         }
       }
+      // after an error: every load issued and not yet waited for lands
+      // before the CTA may exit
+      if (lane == 0 && !ok)
+        for (int k = next_wait; k < next_issue; k += NQ)
+          (void)ptx::mbar_wait_bounded(&xfull_bar[k % XS], (k / XS) & 1, p.timeout_ns);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ----------------------------------------------------------- epilogue
     const int epi_tid = threadIdx.x - 128;
     const int quarter = warp & 3;

@@ -656,8 +656,12 @@ fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUt
 // ---------------------------------------------------------- decode GEMM
 // Block-scaled GEMMs of up to 32 tokens run transposed (decode.cuh): one
 // cluster of S CTAs per 128-row weight tile, S the largest power of two up to
-// 8 that keeps every CTA resident at once (two per SM, one for the fused
-// variant) and at least one K block per CTA.
+// 8 with at least one K block per CTA and a grid the SMs hold in one wave
+// (two CTAs per SM where the kernel's ~100 KB of shared memory and <= 128
+// registers let the hardware place two, else one).  The occupancy
+// query reports one CTA per SM for any kernel that allocates tensor memory,
+// so it is not asked: the clusters do not depend on one another, and a grid
+// larger than the SMs hold still completes.
 constexpr int kDecodeMaxM = 32;
 
 template <int MT, int OUT, bool SPLIT, bool FUSED>
@@ -667,10 +671,8 @@ fp8s_status launch_decode_cfg(const CUtensorMap& mw, const CUtensorMap& mx, cons
   auto kern = fp8_decode_kernel<MT, OUT, SPLIT, FUSED>;
   static bool attr_set[kMaxDevices] = {};
   if (fp8s_status s = ensure_smem_attr(kern, Cfg::kSmemBytes, attr_set)) return s;
-  if constexpr (SPLIT) {
-    const int cmax = max_active_clusters(kern, Cfg::kThreads, Cfg::kSmemBytes, splits, dev, info.sms);
-    if (cmax < p.tiles_n) return FP8S_ERR_SHAPE;   // every cluster must be resident (they exchange partials)
-  }
+  (void)info;
+  (void)dev;
   return launch_ex(kern, static_cast<unsigned>(p.tiles_n * splits), Cfg::kThreads, Cfg::kSmemBytes, st,
                    SPLIT ? splits : 1, mw, mx, p);
 }
@@ -678,16 +680,15 @@ fp8s_status launch_decode_cfg(const CUtensorMap& mw, const CUtensorMap& mx, cons
 template <int MT, int OUT, bool FUSED>
 fp8s_status dispatch_decode(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, const DeviceInfo& info,
                             int dev, cudaStream_t st) {
-  constexpr int kPerSm = DecCfg<MT, true, FUSED>::kCtasPerSm;
+  const int64_t slots = DecCfg<MT, true, FUSED>::kCtasPerSm * static_cast<int64_t>(info.sms);
   int s = 8;
-  while (s > 1 && (s > p.num_kb || static_cast<int64_t>(p.tiles_n) * s > kPerSm * static_cast<int64_t>(info.sms))) s /= 2;
-  for (; s > 1; s /= 2) {
-    const fp8s_status r = s == 8   ? launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 8, info, dev, st)
-                          : s == 4 ? launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 4, info, dev, st)
-                                   : launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 2, info, dev, st);
-    if (r != FP8S_ERR_SHAPE) return r;   // else: fewer clusters fit than the count assumed
+  while (s > 1 && (s > p.num_kb || static_cast<int64_t>(p.tiles_n) * s > slots)) s /= 2;
+  switch (s) {
+    case 8: return launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 8, info, dev, st);
+    case 4: return launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 4, info, dev, st);
+    case 2: return launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 2, info, dev, st);
+    default: return launch_decode_cfg<MT, OUT, false, FUSED>(mw, mx, p, 1, info, dev, st);
   }
-  return launch_decode_cfg<MT, OUT, false, FUSED>(mw, mx, p, 1, info, dev, st);
 }
 
 // qa/x: the E4M3 activation (unfused) or the FP16/BF16 one (fused).

@@ -225,26 +225,34 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // The fused linear's activation quantizer for one warp: rows [r0, r0 + 16)
-// of an FP16/BF16 box in shared memory (256-byte rows at xs; rows at or past
-// `rows` are not read) become 1x128 token groups.  Half a warp holds a row
-// (16-byte loads, eight rows a half), the amax is reduced by shuffles on
-// pairs of rows packed into one word, lane l (< 16) computes the scale and
-// reciprocal of row r0 + l (one divide and one reciprocal for all sixteen
-// rows), and the half-warps take their rows' s and y back by shuffle; the
-// elements then follow the quantizers' division path (bit-identical).  The
-// E4M3 bytes go to the MMA's 128-byte swizzled tile at as (16-byte unit u of
-// row r at u ^ (r % 8)), s to sa_rows[r]; if qo is set, also the bytes to
+// of an FP16/BF16 box in shared memory (256-byte rows at xs, at least
+// r0 + 16 of them; rows at or past `rows` count as zero and are not stored)
+// become 1x128 token groups.  Half a warp holds a row (16-byte loads, eight
+// rows a half), the amax is reduced by shuffles on pairs of rows packed into
+// one word, lane l (< 16) computes the scale and reciprocal of row r0 + l
+// (one divide and one reciprocal for all sixteen rows), and the half-warps
+// take their rows' s and y back by shuffle; the elements then follow the
+// quantizers' division path (bit-identical), the IEEE-divide fallback taken
+// for all sixteen rows if any of them needs it.  No branch depends on a row,
+// so the eight rows' work interleaves.  The E4M3 bytes go to the MMA's
+// 128-byte swizzled tile at as (16-byte unit u of row r at u ^ (r % 8)), s
+// to sa_rows[r] (shared memory); if qo is set, also the bytes to
 // qo + r * qld and s to so[r].
 template <int DT>
-__device__ __forceinline__ void quant_box16_rows(uint32_t xs, uint32_t as, int r0, int rows, int lane, float* sa_rows,
-                                                 uint8_t* qo, int64_t qld, float* so) {
+__device__ __forceinline__ void quant_box16_rows(uint32_t xs, uint32_t as, int r0, int rows, int lane,
+                                                 float* sa_rows, uint8_t* qo, int64_t qld, float* so) {
   const int half = lane >> 4, hl = lane & 15;
   uint4 v[8];
   uint32_t a[8];
 #pragma unroll
+  for (int q = 0; q < 8; ++q) v[q] = lds128(xs + static_cast<uint32_t>((r0 + 2 * q + half) * 256 + hl * 16));
+#pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const int r = r0 + 2 * q + half;
-    v[q] = r < rows ? lds128(xs + static_cast<uint32_t>(r * 256 + hl * 16)) : make_uint4(0u, 0u, 0u, 0u);
+    const bool live = r0 + 2 * q + half < rows;
+    v[q].x = live ? v[q].x : 0u;
+    v[q].y = live ? v[q].y : 0u;
+    v[q].z = live ? v[q].z : 0u;
+    v[q].w = live ? v[q].w : 0u;
     a[q] = amax_bits8(v[q]);
   }
 #pragma unroll
@@ -259,28 +267,45 @@ __device__ __forceinline__ void quant_box16_rows(uint32_t xs, uint32_t as, int r
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const uint32_t t = __shfl_sync(0xFFFFFFFFu, a[q], (lane & 1) << 4);
-    if ((lane >> 1) == q) mine = t;
+    mine = (lane >> 1) == q ? t : mine;
   }
-  const UnitScale own(mag_to_float<DT>(mine));
-  uint2 q8[8];
-  float sq[8];
+  const UnitScale own(mag_to_float<DT>(mine));   // lanes 16-31: amax 0, s = 1
+  float sq[8], yq[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const float s = __shfl_sync(0xFFFFFFFFu, own.s, 2 * q + half);
-    const float y = __shfl_sync(0xFFFFFFFFu, own.y, 2 * q + half);
-    const UnitScale us(s, y, !(s >= 0x1p-90f));   // as UnitScale(amax) computes them
-    q8[q] = quant8<DT>(v[q], us);
-    sq[q] = s;
+    sq[q] = __shfl_sync(0xFFFFFFFFu, own.s, 2 * q + half);
+    yq[q] = __shfl_sync(0xFFFFFFFFu, own.y, 2 * q + half);
+  }
+  // UnitScale(s, y, ...) recomputes ylo exactly as UnitScale(amax) does
+  uint2 q8[8];
+  if (__any_sync(0xFFFFFFFFu, own.exact_div)) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) q8[q] = quant8<DT>(v[q], UnitScale(sq[q], yq[q], !(sq[q] >= 0x1p-90f)));
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) q8[q] = quant8_impl<DT, false>(v[q], UnitScale(sq[q], yq[q], false));
   }
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int r = r0 + 2 * q + half;
-    if (r < rows) {
-      const uint32_t unit = static_cast<uint32_t>(hl >> 1) ^ static_cast<uint32_t>(r & 7);
-      const uint32_t dst = as + static_cast<uint32_t>(r * 128) + (unit << 4) + static_cast<uint32_t>((hl & 1) * 8);
-      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(q8[q].x), "r"(q8[q].y) : "memory");
-      if (hl == 0) sa_rows[r] = sq[q];
-      if (qo != nullptr) {
+    const uint32_t unit = static_cast<uint32_t>(hl >> 1) ^ static_cast<uint32_t>(r & 7);
+    const uint32_t dst = as + static_cast<uint32_t>(r * 128) + (unit << 4) + static_cast<uint32_t>((hl & 1) * 8);
+    const uint32_t sdst = ptx::smem_u32(sa_rows + r);
+    asm volatile(
+        "{\n\t.reg .pred p, h, ps;\n\t"
+        "setp.lt.s32 p, %3, %4;\n\t"
+        "setp.eq.s32 h, %7, 0;\n\t"
+        "@p st.shared.v2.u32 [%0], {%1, %2};\n\t"
+        "and.pred ps, p, h;\n\t"
+        "@ps st.shared.f32 [%5], %6;\n\t}" ::"r"(dst),
+        "r"(q8[q].x), "r"(q8[q].y), "r"(r), "r"(rows), "r"(sdst), "f"(sq[q]), "r"(hl)
+        : "memory");
+  }
+  if (qo != nullptr) {   // warp-uniform
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int r = r0 + 2 * q + half;
+      if (r < rows) {
         reinterpret_cast<uint2*>(qo + static_cast<int64_t>(r) * qld)[hl] = q8[q];
         if (hl == 0) so[r] = sq[q];
       }
