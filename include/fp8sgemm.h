@@ -268,13 +268,17 @@ FP8S_API fp8s_status fp8_e5m2_decode(const uint8_t* q, int64_t numel, void* y, f
  *   qa, sa  both NULL, or qa [M][K] E4M3 and sa [K/128][M] FP32 outputs that
  *       receive the quantized activation and its scales (byte- and
  *       bit-identical to fp8_quantize_token_group's).
- * Designed for decode batches (M <= 128; M <= 16 uses a 16-row activation
- * box), where the weight stream dominates; any M is correct, but above 16
- * rows every CTA of a row of output tiles repeats the quantization of its
- * activation tile, so the two-call path (fp8_quantize_token_group, then
- * fp8_gemm_scaled) is faster there.  Tile overrides (fp8s_gemm_override)
- * apply with bn 64 or 128 (any split), or bn 192 (split only for M <= 16),
- * and no pair; others give FP8S_ERR_SHAPE.
+ * M <= 32 without a tile override runs the transposed decode kernel (the
+ * weight tile as the MMA's 128-row operand, the M tokens as its 16 or 32
+ * columns); larger M, or a call with an override, runs the general kernel
+ * on 128-row activation boxes.  Any M is correct.  Every CTA quantizes the
+ * activation of its own K range, so a row of output tiles repeats that
+ * work: on a B300 the two-call path (fp8_quantize_token_group, then
+ * fp8_gemm_scaled) was faster for every measured shape (Llama-2-7B linears
+ * at M = 1..16: ~1.4x its time; at M = 128 several times), and this entry
+ * point is the one-launch form, not the fast one.  Tile overrides
+ * (fp8s_gemm_override) apply with bn 64 or 128 (any split), or bn 192
+ * (split only for M <= 16), and no pair; others give FP8S_ERR_SHAPE.
  * All pointers 16-byte aligned.  One kernel launch.
  */
 FP8S_API fp8s_status fp8_linear_token_group(const void* x, fp8s_dtype xt, int64_t M, int64_t K, const uint8_t* qw,
