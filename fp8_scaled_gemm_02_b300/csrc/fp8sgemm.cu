@@ -664,6 +664,15 @@ fp8s_status dispatch_gemm(const GemmChoice& ch, const CUtensorMap& ma, const CUt
 // larger than the SMs hold still completes.
 constexpr int kDecodeMaxM = 32;
 
+// Splits of the decode kernel's K range: the largest power of two up to 8
+// with at least one K block per CTA and tiles * S <= slots (CTAs the SMs
+// hold at once).
+int decode_splits(int64_t tiles, int num_kb, int64_t slots) {
+  int s = 8;
+  while (s > 1 && (s > num_kb || tiles * s > slots)) s /= 2;
+  return s;
+}
+
 template <int MT, int OUT, bool SPLIT, bool FUSED>
 fp8s_status launch_decode_cfg(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, int splits,
                               const DeviceInfo& info, int dev, cudaStream_t st) {
@@ -680,9 +689,7 @@ fp8s_status launch_decode_cfg(const CUtensorMap& mw, const CUtensorMap& mx, cons
 template <int MT, int OUT, bool FUSED>
 fp8s_status dispatch_decode(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, const DeviceInfo& info,
                             int dev, cudaStream_t st) {
-  const int64_t slots = DecCfg<MT, true, FUSED>::kCtasPerSm * static_cast<int64_t>(info.sms);
-  int s = 8;
-  while (s > 1 && (s > p.num_kb || static_cast<int64_t>(p.tiles_n) * s > slots)) s /= 2;
+  const int s = decode_splits(p.tiles_n, p.num_kb, DecCfg<MT, true, FUSED>::kCtasPerSm * static_cast<int64_t>(info.sms));
   switch (s) {
     case 8: return launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 8, info, dev, st);
     case 4: return launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 4, info, dev, st);
@@ -1049,6 +1056,14 @@ fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode
   if (!bn || !splits || !pair) return FP8S_ERR_NULL;
   if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || sms < 1) return FP8S_ERR_SHAPE;
   if ((mode == FP8S_SCALE_BLOCK || mode == FP8S_SCALE_BLOCK_UE8M0) && K % 128 != 0) return FP8S_ERR_SHAPE;
+  if (mode == FP8S_SCALE_BLOCK && M <= kDecodeMaxM) {
+    // the transposed decode kernel: 128 output columns a tile, split-K
+    *bn = kBM;
+    *splits = decode_splits((N + kBM - 1) / kBM, static_cast<int>(K / kBK),
+                            DecCfg<16, true, false>::kCtasPerSm * static_cast<int64_t>(sms));
+    *pair = 0;
+    return FP8S_OK;
+  }
   const GemmChoice ch = choose_gemm(M, N, (K + kBK - 1) / kBK, mode, sms);
   *bn = ch.bn;
   *splits = ch.splits;

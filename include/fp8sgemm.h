@@ -203,6 +203,11 @@ FP8S_API fp8s_status fp8_quantize_weight_block(const void* w, fp8s_dtype wt, int
  *        accumulated in FP32.  K % 128 == 0.  Codes of 255 (NaN) are not
  *        accepted.
  *   M, N >= 1, K >= 16.  N need not be a multiple of anything.
+ * Block mode with M <= 32 (and no tile override) runs a decode kernel that
+ * computes C^T = qb . qa^T: each 128-row weight tile is the MMA's 128-row
+ * operand and the M tokens its 16 or 32 columns, the tile's K range split
+ * over a thread-block cluster (partials exchanged through distributed
+ * shared memory and summed in rank order, so results are deterministic).
  */
 FP8S_API fp8s_status fp8_gemm_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                             void* c, fp8s_dtype ct, int64_t M, int64_t N, int64_t K,
@@ -310,6 +315,8 @@ FP8S_API fp8s_status fp8s_gemm_override(int bn, int splits, int pair);
  * tile through tcgen05 cta_group::2).  Host-only and side-effect free; no
  * GPU is needed.  Same shape rules and status codes as fp8_gemm_scaled.  (At
  * run time a split that the device cannot hold falls back to splits = 1.)
+ * For FP8S_SCALE_BLOCK with M <= 32 it describes the decode kernel:
+ * *bn = 128 output columns per tile, *splits its split-K, *pair = 0.
  */
 FP8S_API fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode, int sms, int* bn,
                                     int* splits, int* pair);

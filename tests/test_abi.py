@@ -186,6 +186,22 @@ def test_gemm_plan_matches_measured_choices(lib):
     assert sp == 1 and pr == 0
 
 
+def test_gemm_plan_decode_batches(lib):
+    """Block mode with M <= 32 runs the transposed decode kernel: 128 output
+    columns a tile, K split over the largest power-of-two cluster (<= 8) with
+    tiles * splits <= 2 * SMs and at least one K block a CTA."""
+    BLOCK, UE8 = 1, 3
+    assert plan(lib, 1, 12288, 4096, BLOCK) == (128, 2, 0)     # 96 tiles: 192 CTAs
+    assert plan(lib, 16, 4096, 4096, BLOCK) == (128, 8, 0)     # 32 tiles: 256 CTAs
+    assert plan(lib, 32, 4096, 11008, BLOCK) == (128, 8, 0)
+    assert plan(lib, 8, 22016, 4096, BLOCK) == (128, 1, 0)     # 172 tiles: no split
+    assert plan(lib, 1, 100, 256, BLOCK) == (128, 2, 0)        # two K blocks: at most two splits
+    assert plan(lib, 1, 100, 128, BLOCK) == (128, 1, 0)
+    # UE8M0 mode has no decode kernel: the general kernel's plan at any M
+    bn, sp, pr = plan(lib, 1, 4096, 4096, UE8)
+    assert pr == 0 and bn in (32, 64, 128, 192, 256)
+
+
 def test_gemm_plan_argument_checks(lib):
     bn, sp, pr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     args = (ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(pr))
