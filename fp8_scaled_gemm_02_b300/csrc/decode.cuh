@@ -44,17 +44,23 @@
 
 namespace fp8s {
 
-template <int MT, bool SPLIT, bool FUSED>
+// FUSED: 0 = the E4M3 activation comes quantized; 1 = fused, the activation
+// streamed through a ring of its own and quantized K block by K block; 2 =
+// fused, the CTA's whole K range of the activation quantized once into a
+// resident shared-memory buffer before the MMAs start.
+template <int MT, bool SPLIT, int FUSED>
 struct DecCfg {
+  static constexpr bool kRing = FUSED == 1;
+  static constexpr bool kRes = FUSED == 2;
   static_assert(MT == 16 || MT == 32, "token columns per MMA");
   static constexpr int kEpiWarps = 4;
   // Two CTAs per SM (~100 KB of shared memory, <= 128 registers) for the
   // unfused kernel and the fused MT = 16 one; the fused MT = 32 kernel takes
   // an SM alone.  Fused: kQWarps quantizer warps, 2-3 and 8.. (the epilogue
   // keeps warps 4-7, whose warp index modulo 4 is their TMEM lane quarter).
-  static constexpr int kCtasPerSm = (FUSED && MT == 32) ? 1 : 2;
-  static constexpr int kQWarps = FUSED ? (MT == 16 ? 2 : 4) : 0;
-  static constexpr int kThreads = 128 + 32 * kEpiWarps + (FUSED ? 32 * (kQWarps - 2) : 0);
+  static constexpr int kCtasPerSm = (kRing && MT == 32) ? 1 : 2;
+  static constexpr int kQWarps = kRing ? (MT == 16 ? 2 : 4) : 0;
+  static constexpr int kThreads = 128 + 32 * kEpiWarps + (kRing ? 32 * (kQWarps - 2) : 0);
   static constexpr int kWBytes = kBM * kBK;                 // 128 weight rows x one K block
   static constexpr int kXBytes = MT * kBK;                  // E4M3 activation rows
   // Unfused: a stage holds the weight tile and the E4M3 activation tile.
@@ -62,24 +68,31 @@ struct DecCfg {
   // its own, kXSlots slots of [FP16/BF16 box (MT x 256 B) | E4M3 tile
   // (MT x 128 B)], slot j owned by quantizer j % kQWarps.
   static constexpr int kStageBytes = FUSED ? kWBytes : kWBytes + kXBytes;
+  // resident (FUSED == 2): up to kActKb K blocks of E4M3 activation tiles
+  // and their token scales, for the CTA's whole K range
+  static constexpr int kActKb = kRes ? (MT == 16 ? 16 : 8) : 0;
+  static constexpr int kActBytes = kActKb * MT * kBK;
+  static constexpr int kSaBufBytes = kActKb * MT * 4;
   static constexpr int kXSlots = 2 * kQWarps;
   static constexpr int kX16Bytes = MT * kBK * 2;
-  static constexpr int kXSlotBytes = FUSED ? kX16Bytes + kXBytes : 0;
+  static constexpr int kXSlotBytes = kRing ? kX16Bytes + kXBytes : 0;
   static constexpr int kXRingBytes = kXSlots * kXSlotBytes;
   static constexpr int kPitch = MT + 4;                     // staging row pitch (floats): 16-byte rows
   static constexpr int kStagingBytes = kBM * kPitch * 4;
   static constexpr int kRecvBytes = SPLIT ? 112 * kPitch * 4 : 0;
-  static constexpr int kSaSlots = FUSED ? 12 : 0;           // fused: token scales per K block
+  static constexpr int kSaSlots = kRing ? 12 : 0;            // ring: token scales per K block
   static constexpr int kSaBytes = kSaSlots * MT * 4;
   static constexpr int kBudget = kCtasPerSm == 2 ? 104 * 1024 : 220 * 1024;
-  static constexpr int kStagesRaw = (kBudget - kXRingBytes - kRecvBytes - kSaBytes - 1024) / kStageBytes;
+  static constexpr int kStagesRaw =
+      (kBudget - kXRingBytes - kActBytes - kSaBufBytes - kRecvBytes - kSaBytes - 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(!SPLIT || kStages * kStageBytes >= kStagingBytes, "staging fits in the ring");
   static constexpr int kNBuf = 8;
   static constexpr int kTmemCols = kNBuf * MT;               // 128 or 256: a power of two
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 3 + (FUSED ? 3 * kXSlots + 2 * kSaSlots : 0)) + 16;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kXRingBytes + kRecvBytes + kSaBytes + kBarBytes;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNBuf + 4 + (kRing ? 3 * kXSlots + 2 * kSaSlots : 0)) + 16;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + kXRingBytes + kActBytes + kSaBufBytes + kRecvBytes + kSaBytes + kBarBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   // A quantizer runs at most kXSlots K blocks ahead of the MMA, which runs at
   // most kNBuf ahead of the epilogue; with 2 * kSaSlots above that lead no
@@ -104,7 +117,7 @@ __device__ __forceinline__ void dec_reduce(const float* send, const float* recv,
     src[q] = q == static_cast<int>(rank) ? send + static_cast<int>(rank) * R * kPitch
                                          : recv + (q < static_cast<int>(rank) ? q : q - 1) * R * kPitch;
   const int mmax = p.M < MT ? p.M : MT;
-  for (int idx = tid; idx < R * mmax; idx += 32 * DecCfg<MT, true, false>::kEpiWarps) {
+  for (int idx = tid; idx < R * mmax; idx += 32 * DecCfg<MT, true, 0>::kEpiWarps) {
     const int m = idx / R, rr = idx - (idx / R) * R;
     float v[S];
 #pragma unroll
@@ -117,7 +130,7 @@ __device__ __forceinline__ void dec_reduce(const float* send, const float* recv,
   }
 }
 
-template <int MT, int OUT, bool SPLIT, bool FUSED>
+template <int MT, int OUT, bool SPLIT, int FUSED>
 __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT, SPLIT, FUSED>::kCtasPerSm)
     fp8_decode_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                       const GemmParams p) {
@@ -131,10 +144,12 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
   constexpr int XS = Cfg::kXSlots > 0 ? Cfg::kXSlots : 1;   // (unfused: no activation slots)
   uint8_t* w_ring = smem;
   uint8_t* x_ring = w_ring + S_ * Cfg::kWBytes;             // unfused: E4M3 tiles, one per stage
-  uint8_t* xq_ring = smem + S_ * Cfg::kStageBytes;          // fused: activation slots
+  uint8_t* xq_ring = smem + S_ * Cfg::kStageBytes;          // ring: activation slots
+  uint8_t* act_buf = xq_ring + Cfg::kXRingBytes;            // resident: E4M3 tiles, K block i at i * MT * 128
+  float* sa_buf = reinterpret_cast<float*>(act_buf + Cfg::kActBytes);   // resident: [i][MT] token scales
   float* staging = reinterpret_cast<float*>(smem);  // split-K: after the ring has drained
-  const float* recv = reinterpret_cast<const float*>(xq_ring + Cfg::kXRingBytes);
-  float* sa_ring = reinterpret_cast<float*>(xq_ring + Cfg::kXRingBytes + Cfg::kRecvBytes);
+  const float* recv = reinterpret_cast<const float*>(act_buf + Cfg::kActBytes + Cfg::kSaBufBytes);
+  float* sa_ring = reinterpret_cast<float*>(act_buf + Cfg::kActBytes + Cfg::kSaBufBytes + Cfg::kRecvBytes);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sa_ring) + Cfg::kSaBytes);
   uint64_t* empty_bar = full_bar + S_;
   uint64_t* tfull_bar = empty_bar + S_;
@@ -142,10 +157,11 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
   uint64_t* mma_done_bar = tempty_bar + NBUF;
   uint64_t* staged_bar = mma_done_bar + 1;
   uint64_t* recv_bar = staged_bar + 1;
-  uint64_t* x8_ready_bar = recv_bar + 1;                          // fused: slot's E4M3 rows written
-  uint64_t* xfull_bar = x8_ready_bar + (FUSED ? XS : 0);          // fused: slot's activation box landed
-  uint64_t* xempty_bar = xfull_bar + (FUSED ? XS : 0);            // fused: slot's MMAs done
-  uint64_t* sa_full_bar = xempty_bar + (FUSED ? XS : 0);          // fused: a scale slot written
+  uint64_t* act_ready_bar = recv_bar + 1;                        // resident: the activation is quantized
+  uint64_t* x8_ready_bar = act_ready_bar + 1;                     // ring: slot's E4M3 rows written
+  uint64_t* xfull_bar = x8_ready_bar + (Cfg::kRing ? XS : 0);     // ring: slot's activation box landed
+  uint64_t* xempty_bar = xfull_bar + (Cfg::kRing ? XS : 0);       // ring: slot's MMAs done
+  uint64_t* sa_full_bar = xempty_bar + (Cfg::kRing ? XS : 0);     // ring: a scale slot written
   uint64_t* sa_free_bar = sa_full_bar + Cfg::kSaSlots;            // fused: a scale slot read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sa_free_bar + Cfg::kSaSlots);
 
@@ -177,7 +193,8 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
     ptx::mbar_init(mma_done_bar, 1);
     ptx::mbar_init(staged_bar, Cfg::kEpiWarps);
     ptx::mbar_init(recv_bar, 1);
-    if constexpr (FUSED) {
+    ptx::mbar_init(act_ready_bar, 6);   // resident: quantizer warps 2-7
+    if constexpr (Cfg::kRing) {
       for (int j = 0; j < XS; ++j) {
         ptx::mbar_init(&x8_ready_bar[j], 1);   // the slot's quantizer warp
         ptx::mbar_init(&xfull_bar[j], 1);
@@ -194,7 +211,14 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
     ptx::tmem_alloc<Cfg::kTmemCols>(tmem_slot);
     ptx::tmem_relinquish();
   }
-  if constexpr (FUSED) {
+  if constexpr (Cfg::kRes) {
+    // rows past M are never written by the quantizers: zero bytes, scale 0
+    for (int i = threadIdx.x; i < Cfg::kActBytes / 16; i += Cfg::kThreads)
+      ptx::sts128(ptx::smem_u32(act_buf) + 16u * static_cast<uint32_t>(i), 0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < Cfg::kActKb * MT; i += Cfg::kThreads) sa_buf[i] = 0.0f;
+    ptx::fence_proxy_async_shared();
+  }
+  if constexpr (Cfg::kRing) {
     // activation rows past M are never written by the quantizer: they stay
     // zero, and their token scales 0 (the products they meet are zero)
     for (int i = threadIdx.x; i < XS * Cfg::kXBytes / 16; i += Cfg::kThreads) {
@@ -216,6 +240,71 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
 
   // fused: the box holds the M token rows (M <= MT), 256 bytes each
   const uint32_t x16_box_bytes = static_cast<uint32_t>(p.M < MT ? p.M : MT) * kBK * 2u;
+
+  // Resident: warps 2-7 quantize the CTA's whole K range of the activation
+  // once, straight from global memory, while the producer already streams
+  // the weight.  A lane takes half a 1x128 token group (64 elements: eight
+  // 16-byte loads); its partner lane (the other half) completes the amax by
+  // one shuffle; both compute s = fl32(amax / 448) and its reciprocal pair,
+  // and the lane casts its 64 elements with the token-group quantizer's
+  // arithmetic ([P5] groups, [P2] s3 steps 2-4; bit-identical) into four
+  // 16-byte units of the K block's swizzled E4M3 tile (unit u of row m at
+  // u ^ (m % 8)); the first half's lane stores s.  K block i of the CTA's
+  // issue order sits at act_buf + i * MT * 128, its scales at sa_buf[i][m].
+  auto res_quantize = [&]() {
+    if constexpr (Cfg::kRes) {
+      const int qw = warp - 2;   // 0..5
+      // the host launches this form only when nkb <= kActKb; beyond that
+      // nothing is written outside the buffer and the error word says so
+      const int nkb_q = nkb <= Cfg::kActKb ? nkb : Cfg::kActKb;
+      if (nkb > Cfg::kActKb && qw == 0 && lane == 0) record_error(kErrProducer);
+      const int units = 2 * p.M * nkb_q;
+      const uint16_t* X = reinterpret_cast<const uint16_t*>(p.x);
+      const bool copy_out = p.qa_out != nullptr && tn == 0;
+      for (int base = 32 * qw; base < units; base += 6 * 32) {   // warp-uniform
+        const int u = base + lane;
+        const bool live = u < units;   // units is even: partners are live together
+        const int i = live ? u / (2 * p.M) : 0;
+        const int rem = u - i * 2 * p.M;
+        const int m = live ? rem >> 1 : 0, h = rem & 1;
+        const int kb = kb_at(i);
+        uint4 v[8];
+        uint32_t a = 0;
+        if (live) {
+          const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * p.K + kb * kBK + h * 64);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[j] = __ldg(src + j);
+            a = max(a, amax_bits8(v[j]));
+          }
+        }
+        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        if (live) {
+          const UnitScale us(mag_to_float<DT>(a));
+          uint2 q[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) q[j] = quant8<DT>(v[j], us);
+          const uint32_t row = ptx::smem_u32(act_buf) + static_cast<uint32_t>(i * MT * kBK + m * kBK);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t unit = static_cast<uint32_t>(h * 4 + c) ^ static_cast<uint32_t>(m & 7);
+            ptx::sts128(row + (unit << 4), q[2 * c].x, q[2 * c].y, q[2 * c + 1].x, q[2 * c + 1].y);
+          }
+          if (h == 0) sa_buf[i * MT + m] = us.s;
+          if (copy_out) {
+            uint4* dst = reinterpret_cast<uint4*>(p.qa_out + static_cast<int64_t>(m) * p.K + kb * kBK + h * 64);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(q[2 * c].x, q[2 * c].y, q[2 * c + 1].x, q[2 * c + 1].y);
+            if (h == 0) p.sa_out[static_cast<int64_t>(kb) * p.M + m] = us.s;
+          }
+        }
+      }
+      ptx::fence_proxy_async_shared();   // the E4M3 tiles, before the MMA reads them
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(act_ready_bar);
+    }
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -245,31 +334,39 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBM, MT);
       const uint32_t w0 = ptx::smem_u32(w_ring), x0 = ptx::smem_u32(x_ring), xq0 = ptx::smem_u32(xq_ring);
-      for (int i = 0; i < nkb; ++i) {
+      const uint32_t act0 = ptx::smem_u32(act_buf);
+      bool act_ok = true;
+      if constexpr (Cfg::kRes) act_ok = ptx::mbar_wait_bounded(act_ready_bar, 0, p.timeout_ns);
+      for (int i = 0; i < nkb && act_ok; ++i) {
         const int buf = i % NBUF, s = i % S_;
-        const int xj = FUSED ? i % XS : 0;
+        const int xj = Cfg::kRing ? i % XS : 0;
         if (!ptx::mbar_wait_bounded(&tempty_bar[buf], ((i / NBUF) & 1) ^ 1, p.timeout_ns) ||
             !ptx::mbar_wait_bounded(&full_bar[s], (i / S_) & 1, p.timeout_ns) ||
-            (FUSED && !ptx::mbar_wait_bounded(&x8_ready_bar[xj], (i / XS) & 1, p.timeout_ns))) {
+            (Cfg::kRing && !ptx::mbar_wait_bounded(&x8_ready_bar[xj], (i / XS) & 1, p.timeout_ns))) {
           record_error(kErrMma);
           break;
         }
         ptx::tc_fence_after();
         const uint64_t adesc = ptx::smem_desc_sw128_kmajor(w0 + s * Cfg::kWBytes);
         const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(
-            FUSED ? xq0 + static_cast<uint32_t>(xj * Cfg::kXSlotBytes + Cfg::kX16Bytes) : x0 + s * Cfg::kXBytes);
+            Cfg::kRes    ? act0 + static_cast<uint32_t>(i * MT * kBK)
+            : Cfg::kRing ? xq0 + static_cast<uint32_t>(xj * Cfg::kXSlotBytes + Cfg::kX16Bytes)
+                         : x0 + s * Cfg::kXBytes);
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * MT);
 #pragma unroll
         for (int k = 0; k < kBK / kMmaK; ++k) ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
         ptx::mma_commit(&empty_bar[s]);
-        if constexpr (FUSED) ptx::mma_commit(&xempty_bar[xj]);
+        if constexpr (Cfg::kRing) ptx::mma_commit(&xempty_bar[xj]);
         ptx::mma_commit(&tfull_bar[buf]);
       }
+      if (!act_ok) record_error(kErrMma);
       ptx::mma_commit(mma_done_bar);
       if (!ptx::mbar_wait_bounded(mma_done_bar, 0, p.timeout_ns)) record_error(kErrMma);
     }
-  } else if (FUSED && (warp == 2 || warp == 3 || warp >= 8)) {
-    // --------------------------------------- fused activation quantizer
+  } else if (Cfg::kRes && (warp == 2 || warp == 3)) {
+    res_quantize();
+  } else if (Cfg::kRing && (warp == 2 || warp == 3 || warp >= 8)) {
+    // ------------------------------- fused activation quantizer (ring)
     // K block i (in the CTA's issue order) goes to quantizer i % kQWarps and
     // activation slot j = i % kXSlots (two slots per quantizer).  A slot's
     // FP16/BF16 box is free again once its quantizer has read it, so the
@@ -281,7 +378,7 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
     // rows at a time into the slot's swizzled E4M3 tile, its scale into the
     // scale-ring slot of this K block.  Every barrier of a slot is waited
     // for and arrived on by its one quantizer, in order.
-    if constexpr (FUSED) {
+    if constexpr (Cfg::kRing) {
       const int qwarp = warp < 4 ? warp - 2 : warp - 6;   // 0 .. kQWarps - 1
       constexpr int NQ = Cfg::kQWarps;
       const bool copy_out = p.qa_out != nullptr && tn == 0;
@@ -346,6 +443,18 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
 #pragma unroll
     for (int j = 0; j < MT / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
     bool ok = true;
+    if constexpr (Cfg::kRes) {
+      // these warps quantize their share of the activation first; every
+      // warp's token scales are in sa_buf once all six have arrived
+      res_quantize();
+      bool got = true;
+      if (lane == 0) got = ptx::mbar_wait_bounded(act_ready_bar, 0, p.timeout_ns);
+      if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
+        if (lane == 0) record_error(kErrEpilogue);
+        ok = false;
+      }
+      __syncwarp();  // lane 0's acquire orders the other lanes' reads too
+    }
     // token scales of the next K block (unfused: from global memory, one K
     // block ahead; the tokens past M get 0)
     float sa_n[MT];
@@ -375,7 +484,17 @@ __global__ void __launch_bounds__(DecCfg<MT, SPLIT, FUSED>::kThreads, DecCfg<MT,
         ok = false;
         break;
       }
-      if constexpr (FUSED) {
+      if constexpr (Cfg::kRes) {
+#pragma unroll
+        for (int m = 0; m < MT; m += 4) {
+          const float4 f = *reinterpret_cast<const float4*>(sa_buf + i * MT + m);
+          sa_c[m] = f.x;
+          sa_c[m + 1] = f.y;
+          sa_c[m + 2] = f.z;
+          sa_c[m + 3] = f.w;
+        }
+      }
+      if constexpr (Cfg::kRing) {
         const int slot = i % Cfg::kSaSlots;
         bool got = true;
         if (lane == 0) got = ptx::mbar_wait_bounded(&sa_full_bar[slot], (i / Cfg::kSaSlots) & 1, p.timeout_ns);

@@ -673,7 +673,7 @@ int decode_splits(int64_t tiles, int num_kb, int64_t slots) {
   return s;
 }
 
-template <int MT, int OUT, bool SPLIT, bool FUSED>
+template <int MT, int OUT, bool SPLIT, int FUSED>
 fp8s_status launch_decode_cfg(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, int splits,
                               const DeviceInfo& info, int dev, cudaStream_t st) {
   using Cfg = DecCfg<MT, SPLIT, FUSED>;
@@ -686,10 +686,12 @@ fp8s_status launch_decode_cfg(const CUtensorMap& mw, const CUtensorMap& mx, cons
                    SPLIT ? splits : 1, mw, mx, p);
 }
 
-template <int MT, int OUT, bool FUSED>
+// s: the split-K (1, 2, 4 or 8); 0 = decode_splits' choice for this kernel.
+template <int MT, int OUT, int FUSED>
 fp8s_status dispatch_decode(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, const DeviceInfo& info,
-                            int dev, cudaStream_t st) {
-  const int s = decode_splits(p.tiles_n, p.num_kb, DecCfg<MT, true, FUSED>::kCtasPerSm * static_cast<int64_t>(info.sms));
+                            int dev, cudaStream_t st, int s = 0) {
+  if (s == 0)
+    s = decode_splits(p.tiles_n, p.num_kb, DecCfg<MT, true, FUSED>::kCtasPerSm * static_cast<int64_t>(info.sms));
   switch (s) {
     case 8: return launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 8, info, dev, st);
     case 4: return launch_decode_cfg<MT, OUT, true, FUSED>(mw, mx, p, 4, info, dev, st);
@@ -727,11 +729,38 @@ fp8s_status run_decode(const void* act, const uint8_t* qw, const float* sa, cons
   p.timeout_ns = kWaitTimeoutNs;
   p.qa_out = qa_out;
   p.sa_out = sa_out;
-  if (ct == FP8S_F16)
-    return mt == 16 ? dispatch_decode<16, kOutF16, FUSED>(mw, mx, p, info, dev, st)
-                    : dispatch_decode<32, kOutF16, FUSED>(mw, mx, p, info, dev, st);
-  return mt == 16 ? dispatch_decode<16, kOutBF16, FUSED>(mw, mx, p, info, dev, st)
-                  : dispatch_decode<32, kOutBF16, FUSED>(mw, mx, p, info, dev, st);
+  p.x = FUSED ? act : nullptr;
+  if constexpr (FUSED) {
+    // The resident form (the CTA's whole K range quantized up front) when
+    // that range fits its activation buffer, with K split further if needed,
+    // one round of its quantizer lanes covers it (2 * M * K blocks <= the
+    // 192 lanes of warps 2-7) and M < 16; else the ring form.  (Measured on
+    // the Llama-2-7B linears: the resident form is faster up to M = 8, the
+    // ring from M = 16.)
+    const int act_kb = mt == 16 ? DecCfg<16, true, 2>::kActKb : DecCfg<32, true, 2>::kActKb;
+    int s = decode_splits(p.tiles_n, p.num_kb, DecCfg<16, true, 2>::kCtasPerSm * static_cast<int64_t>(info.sms));
+    while (s < 8 && 2 * s <= p.num_kb && (p.num_kb + s - 1) / s > act_kb) s *= 2;
+    const int kb_per_cta = (p.num_kb + s - 1) / s;
+    const bool res = kb_per_cta <= act_kb && 2 * M * kb_per_cta <= 6 * 32 && M < 16;
+    if (ct == FP8S_F16) {
+      if (mt == 16)
+        return res ? dispatch_decode<16, kOutF16, 2>(mw, mx, p, info, dev, st, s)
+                   : dispatch_decode<16, kOutF16, 1>(mw, mx, p, info, dev, st);
+      return res ? dispatch_decode<32, kOutF16, 2>(mw, mx, p, info, dev, st, s)
+                 : dispatch_decode<32, kOutF16, 1>(mw, mx, p, info, dev, st);
+    }
+    if (mt == 16)
+      return res ? dispatch_decode<16, kOutBF16, 2>(mw, mx, p, info, dev, st, s)
+                 : dispatch_decode<16, kOutBF16, 1>(mw, mx, p, info, dev, st);
+    return res ? dispatch_decode<32, kOutBF16, 2>(mw, mx, p, info, dev, st, s)
+               : dispatch_decode<32, kOutBF16, 1>(mw, mx, p, info, dev, st);
+  } else {
+    if (ct == FP8S_F16)
+      return mt == 16 ? dispatch_decode<16, kOutF16, 0>(mw, mx, p, info, dev, st)
+                      : dispatch_decode<32, kOutF16, 0>(mw, mx, p, info, dev, st);
+    return mt == 16 ? dispatch_decode<16, kOutBF16, 0>(mw, mx, p, info, dev, st)
+                    : dispatch_decode<32, kOutBF16, 0>(mw, mx, p, info, dev, st);
+  }
 }
 
 // The fused linear: block mode, single-CTA tiles of 64 or 128 columns (with
@@ -1060,7 +1089,7 @@ fp8s_status fp8s_gemm_plan(int64_t M, int64_t N, int64_t K, fp8s_scale_mode mode
     // the transposed decode kernel: 128 output columns a tile, split-K
     *bn = kBM;
     *splits = decode_splits((N + kBM - 1) / kBM, static_cast<int>(K / kBK),
-                            DecCfg<16, true, false>::kCtasPerSm * static_cast<int64_t>(sms));
+                            DecCfg<16, true, 0>::kCtasPerSm * static_cast<int64_t>(sms));
     *pair = 0;
     return FP8S_OK;
   }

@@ -92,6 +92,8 @@ struct GemmParams {
   // tile column 0)
   uint8_t* qa_out;
   float* sa_out;
+  // fused decode with a resident activation: the FP16/BF16 activation [M][K]
+  const void* x;
 };
 
 // FR > 0: the fused linear.  A arrives as FP16/BF16 (the output's type) in

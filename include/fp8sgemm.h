@@ -278,10 +278,10 @@ FP8S_API fp8s_status fp8_e5m2_decode(const uint8_t* q, int64_t numel, void* y, f
  * columns); larger M, or a call with an override, runs the general kernel
  * on 128-row activation boxes.  Any M is correct.  Every CTA quantizes the
  * activation of its own K range, so a row of output tiles repeats that
- * work: on a B300 the two-call path (fp8_quantize_token_group, then
- * fp8_gemm_scaled) was faster for every measured shape (Llama-2-7B linears
- * at M = 1..16: ~1.4x its time; at M = 128 several times), and this entry
- * point is the one-launch form, not the fast one.  Tile overrides
+ * work.  Measured on a B300 against the two-call path
+ * (fp8_quantize_token_group, then fp8_gemm_scaled), Llama-2-7B linears:
+ * on par at M = 1 for qkv and down, slower for o and gate/up, ~1.4x its
+ * time at M = 16 and several times at M = 128.  Tile overrides
  * (fp8s_gemm_override) apply with bn 64 or 128 (any split), or bn 192
  * (split only for M <= 16), and no pair; others give FP8S_ERR_SHAPE.
  * All pointers 16-byte aligned.  One kernel launch.
