@@ -11,21 +11,25 @@
 // tokens as rows), the TMEM partial is 128 x MT, and the promotion of a K
 // block is MT columns per thread: the weight stream sets the pace.
 //
-//   warp 0      TMA producer: 128x128-byte weight tiles and MT x 128-byte
-//               E4M3 activation tiles (or, fused, M x 128 FP16/BF16
-//               activation boxes on a barrier of their own, so that their
-//               quantization overlaps the weight tile's flight), 128-byte
-//               swizzle, a STAGES-deep ring.
+//   warp 0      TMA producer: 128x128-byte weight tiles (and, unfused, the
+//               MT x 128-byte E4M3 activation tiles), 128-byte swizzle, a
+//               STAGES-deep ring.
 //   warp 1      MMA issuer: tcgen05.mma kind::f8f6f4, M = 128, N = MT, four
 //               per K block, a fresh TMEM buffer per K block.
-//   warp 2      TMEM allocation; fused: warps 2-3 and 8-11 quantize the
-//               activation (stage s of the ring belongs to quantizer s % 6;
-//               each row of the box is a 1x128 token group, quantized into
-//               the stage's swizzled E4M3 tile, its scale into a ring the
-//               epilogue reads).
+//   warp 2      TMEM allocation.
 //   warps 4-7   epilogue: thread = one weight row n of the tile (its lane
 //               quarter of TMEM), MT token columns; per K block it adds
 //               partial[n][m] * sa[kb][m] * sb[n/128][kb] into FP32 pairs.
+// Fused (the activation arrives in FP16/BF16 and is quantized per 1x128
+// token group inside the kernel), two forms:
+//   resident    warps 2-7 first quantize the CTA's whole K range of the
+//               activation from global memory into a shared-memory buffer
+//               of E4M3 tiles (and its token scales); the MMA loop then
+//               runs as unfused, with the activation tiles resident.
+//   ring        the activation has a ring of its own: quantizer warps (2-3,
+//               and 8-9 for MT = 32) load its M x 128 boxes by TMA ahead of
+//               the MMA and quantize them into the ring's E4M3 tiles, the
+//               token scales into a second ring the epilogue reads.
 // Split-K: the S CTAs of a cluster share the tile, each a K range; the FP32
 // partials are exchanged through distributed shared memory (rank r owns
 // weight rows [r*128/S, (r+1)*128/S)) and summed in rank order, so results
@@ -33,11 +37,11 @@
 // transposed: for a fixed token the 32 lanes of a warp write 32 consecutive
 // columns.
 //
-// A kernel that holds tensor-memory instructions is resident at one CTA per
-// SM (the occupancy the CUDA runtime reports for it, whatever its registers
-// and shared memory), so each CTA takes a ring of ~200 KB, deep enough to
-// keep an SM's share of the HBM bandwidth in flight.  Every wait is bounded
-// as in gemm.cuh.
+// The CUDA occupancy query reports one CTA per SM for any kernel that
+// allocates tensor memory, but the hardware places two when shared memory
+// and registers allow: the unfused kernel, the resident form and the ring
+// form with MT = 16 keep ~100 KB and <= 128 registers so that two CTAs share
+// an SM.  Every wait is bounded as in gemm.cuh.
 #pragma once
 
 #include "gemm.cuh"
